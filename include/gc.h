@@ -1,0 +1,203 @@
+/*
+ * gc.h -- C ABI of libgc: predicate -> exclusive scan -> scatter on one
+ * GB300 GPU (sm_103a).
+ *
+ * Operations and the passages that define them:
+ *
+ *   gc_exclusive_scan    out[i] = in[0] + ... + in[i-1], out[0] = 0.
+ *                        "scan_2.cu -- Day 32: the work-efficient scan"
+ *                        (scanExclusiveCpu, the CPU reference); the same
+ *                        exclusive semantics as "compaction.cu -- Day 33"
+ *                        (scanTilesExclusive, "rank[i] becomes the number of
+ *                        survivors before i").
+ *   gc_select_if         the elements a predicate keeps, in input order, and
+ *                        their count.  "compaction.cu -- Day 33" (file
+ *                        header: predicate, scan, scatter; compactCpu;
+ *                        scatterCompact) and "The CUDA Handbook, ch. 13:
+ *                        Stream compaction" (Listing 13-17, the single-pass
+ *                        form: the highest-numbered tile writes the total).
+ *   gc_partition         stable two-way partition: kept elements in input
+ *                        order, then rejected ones in input order; one scan
+ *                        addresses both halves through i - rank[i].
+ *                        "compaction.cu -- Day 33" (partitionCpu,
+ *                        scatterPartition).
+ *   gc_split_radix       LSD radix sort by one-bit stable splits, bit-clear
+ *                        first, one split per bit in [begin_bit, end_bit).
+ *                        "CIS 565 Project 2: Stream Compaction" (radix sort
+ *                        built on scan); each split is gc_partition with the
+ *                        predicate "bit b is 0".
+ *   gc_select_if_atomic  the comparison path: the same survivors and count,
+ *                        placed by an atomic counter, in no defined order.
+ *                        "compaction.cu -- Day 33" (compactAtomic).
+ *
+ * Conventions common to every entry point:
+ *
+ *   - Pointers named d_* are device pointers (cudaMalloc / torch memory on
+ *     the current device).  Element pointers must be 4-byte aligned; 16-byte
+ *     aligned element pointers take the vectorised kernels, others a scalar
+ *     variant of the same kernels with identical results.
+ *   - n is an element count, 0 <= n <= GC_MAX_ELEMENTS (2^31 - 1).
+ *   - Every call is asynchronous on `stream` (0 = legacy default stream):
+ *     it enqueues work and returns.  Counts and totals are written to device
+ *     memory on that stream; nothing is copied to the host.  The library
+ *     never allocates device memory and never synchronises, except
+ *     gc_query_device_status.
+ *   - Scratch lives in a caller-owned workspace: d_ws, at least
+ *     gc_workspace_bytes(op, n, dtype) bytes, 256-byte aligned, and
+ *     zero-filled once before its first use (gc_workspace_init does that).
+ *     The library leaves it valid for the next call.  One workspace must not
+ *     be used by two calls that can run at the same time (different streams
+ *     without ordering between them).
+ *   - n == 0: the count / total outputs are set to 0, nothing else runs.
+ *   - Return value: GC_OK if the work was enqueued.  Argument errors are
+ *     detected on the host before anything is enqueued.  GC_ERR_CUDA means a
+ *     CUDA call or launch failed (cudaGetLastError() holds the cause).
+ *     Failures inside a kernel (a look-back wait that gave up) are recorded
+ *     in the workspace and reported by gc_query_device_status.
+ */
+#ifndef GC_H
+#define GC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GC_MAX_ELEMENTS 2147483647u
+
+typedef enum {
+    GC_OK = 0,
+    GC_ERR_INVALID_VALUE = 1,      /* null pointer, n too large, bad enum, bad bit range, overlap */
+    GC_ERR_UNSUPPORTED = 2,        /* predicate not defined for the dtype (ODD/EVEN on float32) */
+    GC_ERR_WORKSPACE_TOO_SMALL = 3,
+    GC_ERR_MISALIGNED = 4,         /* element pointer not 4-byte or workspace not 256-byte aligned */
+    GC_ERR_CUDA = 5,               /* a CUDA runtime call or kernel launch failed */
+    GC_ERR_TIMEOUT = 6,            /* device: a look-back wait gave up (see gc_query_device_status) */
+    GC_ERR_DEVICE_CHECK = 7        /* device: a kernel's own bounds check refused to write */
+} gc_status;
+
+typedef enum { GC_I32 = 0, GC_U32 = 1, GC_F32 = 2 } gc_dtype;
+
+/*
+ * Predicates ("compaction.cu -- Day 33" markNonZero / markEven; "The CUDA
+ * Handbook, ch. 13" isOdd):
+ *   GC_PRED_NONZERO  x != 0.  For float32 the IEEE comparison: +0.0 and -0.0
+ *                    are rejected, NaN, infinities and denormals are kept.
+ *   GC_PRED_ODD      (x & 1) != 0, int32 / uint32 only.
+ *   GC_PRED_EVEN     (x & 1) == 0, int32 / uint32 only.
+ */
+typedef enum { GC_PRED_NONZERO = 0, GC_PRED_ODD = 1, GC_PRED_EVEN = 2 } gc_pred;
+
+typedef enum {
+    GC_OP_EXCLUSIVE_SCAN = 0,
+    GC_OP_SELECT_IF = 1,
+    GC_OP_PARTITION = 2,
+    GC_OP_SPLIT_RADIX = 3,
+    GC_OP_SELECT_IF_ATOMIC = 4
+} gc_op;
+
+/* Static, never NULL, "unknown status" for values outside the enum. */
+const char *gc_status_string(gc_status status);
+
+/* Library version string, static. */
+const char *gc_version(void);
+
+/*
+ * Workspace bytes op needs for n elements of dtype (dtype is ignored for
+ * GC_OP_SPLIT_RADIX, whose keys and payloads are uint32).  Returns 0 for an
+ * unknown op or dtype or n > GC_MAX_ELEMENTS.  A workspace sized for the
+ * largest (op, n) it will serve can be reused by every smaller call.
+ */
+size_t gc_workspace_bytes(gc_op op, size_t n, gc_dtype dtype);
+
+/*
+ * Elements per tile of op's kernel (one CTA's share of the input): a size
+ * that is a multiple of it fills every tile, other sizes leave a ragged last
+ * tile.  Returns 0 for an unknown op.
+ */
+size_t gc_tile_elements(gc_op op);
+
+/* cudaMemsetAsync(d_ws, 0, ws_bytes, stream): prepares a new workspace. */
+gc_status gc_workspace_init(void *d_ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Exclusive scan.  d_in and d_out hold n elements of dtype; d_in == d_out
+ * (in place) is allowed, any other overlap is GC_ERR_INVALID_VALUE.
+ * d_total (nullable) receives in[0] + ... + in[n-1] as one element of dtype.
+ * int32 and uint32 add modulo 2^32 (the same bits).  float32 adds within a
+ * tile in float32 with round-to-nearest and carries the running prefix
+ * between tiles in float64, so the result is within a few float32 ulps of
+ * the exact prefix; the summation order is not sequential.
+ */
+gc_status gc_exclusive_scan(const void *d_in, void *d_out, void *d_total,
+                            size_t n, gc_dtype dtype, void *d_ws,
+                            size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Stable select-if.  d_out must have room for n elements (the worst case);
+ * elements [0, *d_count) are the survivors in input order, the rest of d_out
+ * is untouched.  *d_count is written by the kernel (a uint32 in device
+ * memory).  d_in and d_out must not overlap.
+ */
+gc_status gc_select_if(const void *d_in, void *d_out, uint32_t *d_count,
+                       size_t n, gc_dtype dtype, gc_pred pred, void *d_ws,
+                       size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Stable partition.  d_out (n elements) receives the predicate-true
+ * elements in input order followed by the false ones in input order;
+ * *d_count_true (device uint32) is the size of the first half.  d_in and
+ * d_out must not overlap.  Two kernels: a count of the true elements, then
+ * one pass that scans and scatters both halves.
+ */
+gc_status gc_partition(const void *d_in, void *d_out, uint32_t *d_count_true,
+                       size_t n, gc_dtype dtype, gc_pred pred, void *d_ws,
+                       size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * LSD radix sort by one-bit stable splits over bits [begin_bit, end_bit),
+ * 0 <= begin_bit <= end_bit <= 32, lowest bit first, keys with the bit clear
+ * first.  With [0, 32) the keys come out ascending, equal keys in input
+ * order, and d_vals_out holds the payloads permuted with them.  d_vals_in
+ * and d_vals_out are both NULL (keys only) or both non-NULL.  The result
+ * always lands in d_keys_out / d_vals_out; the intermediate ping-pong
+ * buffers live in the workspace.  An input may equal its output (in place);
+ * any other overlap between the four arrays is GC_ERR_INVALID_VALUE.  An
+ * empty bit range copies.  One histogram kernel, then one split kernel per
+ * bit.
+ */
+gc_status gc_split_radix(const uint32_t *d_keys_in, const uint32_t *d_vals_in,
+                         uint32_t *d_keys_out, uint32_t *d_vals_out, size_t n,
+                         int begin_bit, int end_bit, void *d_ws,
+                         size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * The atomic-counter comparison path: the same survivors and the same
+ * *d_count as gc_select_if, in an order the hardware decides (only the
+ * multiset of d_out[0, *d_count) is defined).  One atomic per warp and row
+ * of 128 elements on a single counter.
+ */
+gc_status gc_select_if_atomic(const void *d_in, void *d_out, uint32_t *d_count,
+                              size_t n, gc_dtype dtype, gc_pred pred,
+                              void *d_ws, size_t ws_bytes,
+                              cudaStream_t stream);
+
+/*
+ * SYNCHRONOUS.  Waits for `stream`, then reads and clears the device-side
+ * error word of the workspace.  Returns GC_OK, GC_ERR_TIMEOUT if a kernel's
+ * look-back wait gave up since the last query, GC_ERR_DEVICE_CHECK if a
+ * kernel found an output range outside its buffer (a corrupted workspace) and
+ * skipped those stores -- in both cases the outputs of that call are
+ * undefined -- or GC_ERR_CUDA if the synchronisation itself failed.
+ */
+gc_status gc_query_device_status(void *d_ws, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GC_H */

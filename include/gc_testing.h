@@ -1,0 +1,36 @@
+/*
+ * gc_testing.h -- test hooks of libgc.  Not for production callers.
+ *
+ * They exist so that the library's failure handling can be exercised on a
+ * real GPU without faulting it: every wait inside a kernel has a time limit
+ * after which the kernel records GC_ERR_TIMEOUT in the workspace and
+ * finishes normally, and this hook makes one wait run out on purpose.
+ */
+#ifndef GC_TESTING_H
+#define GC_TESTING_H
+
+#include "gc.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * gc_select_if with a planted failure: tile 0 is never taken by any CTA, so
+ * tile 1's look-back waits for a status word that nobody writes, gives up
+ * after timeout_ns nanoseconds of device time, records GC_ERR_TIMEOUT in the
+ * workspace error word and lets its successors finish.  Requires at least two
+ * tiles (n > gc_tile_elements(GC_OP_SELECT_IF)).  The output is undefined;
+ * gc_query_device_status then returns GC_ERR_TIMEOUT, and the workspace is
+ * fit for the next call.
+ */
+gc_status gc_testing_select_if_skip_tile0(const void *d_in, void *d_out, uint32_t *d_count,
+                                          size_t n, gc_dtype dtype, gc_pred pred, void *d_ws,
+                                          size_t ws_bytes, uint64_t timeout_ns,
+                                          cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GC_TESTING_H */

@@ -1,0 +1,270 @@
+// api.cu -- the C ABI of libgc (include/gc.h): argument checks on the host,
+// workspace sizing, and dispatch to the launchers.  Nothing here touches the
+// GPU before every argument has been checked, so argument errors are
+// reported without any CUDA call.
+#include <cstring>
+
+#include "../../include/gc.h"
+#include "../../include/gc_testing.h"
+#include "gc_internal.h"
+
+namespace gch {
+
+cudaError_t reset_tiles(uint8_t *ws, size_t tiles, cudaStream_t s, bool skip_first_tile)
+{
+    // [kTileCtrOff, kHeaderBytes) holds only the tile counter (and padding).
+    cudaError_t e = cudaMemsetAsync(ws + kTileCtrOff, 0,
+                                    (kHeaderBytes - kTileCtrOff) + status_bytes(tiles), s);
+    if (e == cudaSuccess && skip_first_tile) e = cudaMemsetAsync(ws + kTileCtrOff, 1, 1, s);
+    return e;
+}
+
+cudaError_t clear_accumulators(uint8_t *ws, cudaStream_t s)
+{
+    // [0, 8) is the error word and its tile; the rest of the header is scratch.
+    return cudaMemsetAsync(ws + 8, 0, kHeaderBytes - 8, s);
+}
+
+int sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (cached[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            v = 148;
+        cached[dev] = v;
+    }
+    return cached[dev];
+}
+
+}  // namespace gch
+
+namespace {
+
+using namespace gch;
+
+bool valid_dtype(int dt) { return dt == GC_I32 || dt == GC_U32 || dt == GC_F32; }
+bool valid_pred(int p) { return p == GC_PRED_NONZERO || p == GC_PRED_ODD || p == GC_PRED_EVEN; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+bool overlap(const void *a, size_t abytes, const void *b, size_t bbytes)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bbytes && y < x + abytes;
+}
+
+gc_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GC_OK : GC_ERR_CUDA; }
+
+// Checks shared by every element-wise entry point.
+gc_status check_common(const void *in, const void *out, size_t n, void *ws, size_t ws_bytes,
+                       gc_op op, gc_dtype dt)
+{
+    if (n > GC_MAX_ELEMENTS) return GC_ERR_INVALID_VALUE;
+    if (!valid_dtype(dt)) return GC_ERR_INVALID_VALUE;
+    if (ws == nullptr) return GC_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GC_ERR_MISALIGNED;
+    if (ws_bytes < gc_workspace_bytes(op, n, dt)) return GC_ERR_WORKSPACE_TOO_SMALL;
+    if (n > 0) {
+        if (in == nullptr || out == nullptr) return GC_ERR_INVALID_VALUE;
+        if (!aligned4(in) || !aligned4(out)) return GC_ERR_MISALIGNED;
+        if (overlap(ws, ws_bytes, in, 4 * n) || overlap(ws, ws_bytes, out, 4 * n))
+            return GC_ERR_INVALID_VALUE;
+    }
+    return GC_OK;
+}
+
+gc_status check_select_like(const void *in, const void *out, const uint32_t *count, size_t n,
+                            gc_dtype dt, gc_pred p, void *ws, size_t ws_bytes, gc_op op)
+{
+    gc_status st = check_common(in, out, n, ws, ws_bytes, op, dt);
+    if (st != GC_OK) return st;
+    if (!valid_pred(p)) return GC_ERR_INVALID_VALUE;
+    if (dt == GC_F32 && p != GC_PRED_NONZERO) return GC_ERR_UNSUPPORTED;
+    if (count == nullptr) return GC_ERR_INVALID_VALUE;
+    if (!aligned4(count)) return GC_ERR_MISALIGNED;
+    if (n > 0 && overlap(in, 4 * n, out, 4 * n)) return GC_ERR_INVALID_VALUE;
+    if (overlap(count, 4, out, 4 * n) || overlap(count, 4, in, 4 * n) ||
+        overlap(count, 4, ws, ws_bytes))
+        return GC_ERR_INVALID_VALUE;
+    return GC_OK;
+}
+
+gc_status select_like(bool atomic, const void *d_in, void *d_out, uint32_t *d_count, size_t n,
+                      gc_dtype dt, gc_pred p, void *d_ws, size_t ws_bytes, cudaStream_t s,
+                      const LaunchOpts &o)
+{
+    const gc_op op = atomic ? GC_OP_SELECT_IF_ATOMIC : GC_OP_SELECT_IF;
+    gc_status st = check_select_like(d_in, d_out, d_count, n, dt, p, d_ws, ws_bytes, op);
+    if (st != GC_OK) return st;
+    if (n == 0) return from_cuda(cudaMemsetAsync(d_count, 0, sizeof(uint32_t), s));
+    if (atomic)
+        return from_cuda(launch_select_atomic(d_in, d_out, d_count, uint32_t(n), dt, p, s));
+    return from_cuda(launch_select(d_in, d_out, d_count, uint32_t(n), dt, p,
+                                   static_cast<uint8_t *>(d_ws), s, o));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gc_status_string(gc_status status)
+{
+    switch (status) {
+    case GC_OK: return "GC_OK";
+    case GC_ERR_INVALID_VALUE: return "GC_ERR_INVALID_VALUE: bad argument";
+    case GC_ERR_UNSUPPORTED: return "GC_ERR_UNSUPPORTED: predicate not defined for this dtype";
+    case GC_ERR_WORKSPACE_TOO_SMALL: return "GC_ERR_WORKSPACE_TOO_SMALL";
+    case GC_ERR_MISALIGNED: return "GC_ERR_MISALIGNED: pointer alignment";
+    case GC_ERR_CUDA: return "GC_ERR_CUDA: CUDA call or launch failed";
+    case GC_ERR_TIMEOUT: return "GC_ERR_TIMEOUT: a look-back wait gave up on the device";
+    case GC_ERR_DEVICE_CHECK: return "GC_ERR_DEVICE_CHECK: a kernel refused an out-of-range store";
+    }
+    return "unknown gc_status";
+}
+
+const char *gc_version(void) { return "libgc 0.1 (sm_103a)"; }
+
+size_t gc_workspace_bytes(gc_op op, size_t n, gc_dtype dtype)
+{
+    if (n > GC_MAX_ELEMENTS) return 0;
+    const size_t status = status_bytes(max_tiles(n));
+    switch (op) {
+    case GC_OP_EXCLUSIVE_SCAN:
+        if (!valid_dtype(dtype)) return 0;
+        return kHeaderBytes + status + (dtype == GC_F32 ? status : 0);
+    case GC_OP_SELECT_IF:
+    case GC_OP_PARTITION:
+    case GC_OP_SELECT_IF_ATOMIC:
+        if (!valid_dtype(dtype)) return 0;
+        return kHeaderBytes + status;
+    case GC_OP_SPLIT_RADIX:
+        return radix_temp_offset(n) + 2 * radix_temp_stride(n);
+    }
+    return 0;
+}
+
+size_t gc_tile_elements(gc_op op)
+{
+    switch (op) {
+    case GC_OP_EXCLUSIVE_SCAN: return scan_tile_elems();
+    case GC_OP_SELECT_IF: return select_tile_elems();
+    case GC_OP_PARTITION: return partition_tile_elems();
+    case GC_OP_SPLIT_RADIX: return split_tile_elems();
+    case GC_OP_SELECT_IF_ATOMIC: return atomic_tile_elems();
+    }
+    return 0;
+}
+
+gc_status gc_workspace_init(void *d_ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (d_ws == nullptr) return GC_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(d_ws) & 255u) != 0) return GC_ERR_MISALIGNED;
+    return from_cuda(cudaMemsetAsync(d_ws, 0, ws_bytes, stream));
+}
+
+gc_status gc_exclusive_scan(const void *d_in, void *d_out, void *d_total, size_t n,
+                            gc_dtype dtype, void *d_ws, size_t ws_bytes, cudaStream_t stream)
+{
+    gc_status st = check_common(d_in, d_out, n, d_ws, ws_bytes, GC_OP_EXCLUSIVE_SCAN, dtype);
+    if (st != GC_OK) return st;
+    if (n > 0 && d_in != d_out && overlap(d_in, 4 * n, d_out, 4 * n)) return GC_ERR_INVALID_VALUE;
+    if (d_total != nullptr) {
+        if (!aligned4(d_total)) return GC_ERR_MISALIGNED;
+        if (overlap(d_total, 4, d_out, 4 * n) || overlap(d_total, 4, d_in, 4 * n) ||
+            overlap(d_total, 4, d_ws, ws_bytes))
+            return GC_ERR_INVALID_VALUE;
+    }
+    if (n == 0)
+        return d_total ? from_cuda(cudaMemsetAsync(d_total, 0, 4, stream)) : GC_OK;
+    return from_cuda(launch_scan(d_in, d_out, d_total, uint32_t(n), dtype,
+                                 static_cast<uint8_t *>(d_ws), stream, LaunchOpts{}));
+}
+
+gc_status gc_select_if(const void *d_in, void *d_out, uint32_t *d_count, size_t n,
+                       gc_dtype dtype, gc_pred pred, void *d_ws, size_t ws_bytes,
+                       cudaStream_t stream)
+{
+    return select_like(false, d_in, d_out, d_count, n, dtype, pred, d_ws, ws_bytes, stream,
+                       LaunchOpts{});
+}
+
+gc_status gc_select_if_atomic(const void *d_in, void *d_out, uint32_t *d_count, size_t n,
+                              gc_dtype dtype, gc_pred pred, void *d_ws, size_t ws_bytes,
+                              cudaStream_t stream)
+{
+    return select_like(true, d_in, d_out, d_count, n, dtype, pred, d_ws, ws_bytes, stream,
+                       LaunchOpts{});
+}
+
+gc_status gc_partition(const void *d_in, void *d_out, uint32_t *d_count_true, size_t n,
+                       gc_dtype dtype, gc_pred pred, void *d_ws, size_t ws_bytes,
+                       cudaStream_t stream)
+{
+    gc_status st = check_select_like(d_in, d_out, d_count_true, n, dtype, pred, d_ws, ws_bytes,
+                                     GC_OP_PARTITION);
+    if (st != GC_OK) return st;
+    if (n == 0) return from_cuda(cudaMemsetAsync(d_count_true, 0, sizeof(uint32_t), stream));
+    return from_cuda(launch_partition(d_in, d_out, d_count_true, uint32_t(n), dtype, pred,
+                                      static_cast<uint8_t *>(d_ws), stream, LaunchOpts{}));
+}
+
+gc_status gc_split_radix(const uint32_t *d_keys_in, const uint32_t *d_vals_in,
+                         uint32_t *d_keys_out, uint32_t *d_vals_out, size_t n, int begin_bit,
+                         int end_bit, void *d_ws, size_t ws_bytes, cudaStream_t stream)
+{
+    gc_status st = check_common(d_keys_in, d_keys_out, n, d_ws, ws_bytes, GC_OP_SPLIT_RADIX, GC_U32);
+    if (st != GC_OK) return st;
+    if (begin_bit < 0 || end_bit > 32 || begin_bit > end_bit) return GC_ERR_INVALID_VALUE;
+    if ((d_vals_in == nullptr) != (d_vals_out == nullptr)) return GC_ERR_INVALID_VALUE;
+    if (n == 0) return GC_OK;
+    const size_t b = 4 * n;
+    if (d_keys_in != d_keys_out && overlap(d_keys_in, b, d_keys_out, b)) return GC_ERR_INVALID_VALUE;
+    if (d_vals_in != nullptr) {
+        if (!aligned4(d_vals_in) || !aligned4(d_vals_out)) return GC_ERR_MISALIGNED;
+        if (d_vals_in != d_vals_out && overlap(d_vals_in, b, d_vals_out, b))
+            return GC_ERR_INVALID_VALUE;
+        const void *keys[2] = {d_keys_in, d_keys_out};
+        const void *vals[2] = {d_vals_in, d_vals_out};
+        for (const void *k : keys)
+            for (const void *v : vals)
+                if (overlap(k, b, v, b)) return GC_ERR_INVALID_VALUE;
+        if (overlap(d_ws, ws_bytes, d_vals_in, b) || overlap(d_ws, ws_bytes, d_vals_out, b))
+            return GC_ERR_INVALID_VALUE;
+    }
+    return from_cuda(launch_split_radix(d_keys_in, d_vals_in, d_keys_out, d_vals_out, uint32_t(n),
+                                        begin_bit, end_bit, static_cast<uint8_t *>(d_ws), stream,
+                                        LaunchOpts{}));
+}
+
+gc_status gc_query_device_status(void *d_ws, cudaStream_t stream)
+{
+    if (d_ws == nullptr) return GC_ERR_INVALID_VALUE;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return GC_ERR_CUDA;
+    uint32_t err = 0;
+    if (cudaMemcpy(&err, d_ws, sizeof err, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GC_ERR_CUDA;
+    if (err != 0) {
+        const uint32_t zero[2] = {0, 0};
+        if (cudaMemcpy(d_ws, zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return GC_ERR_CUDA;
+        return (err == GC_ERR_TIMEOUT || err == GC_ERR_DEVICE_CHECK) ? gc_status(err) : GC_ERR_CUDA;
+    }
+    return GC_OK;
+}
+
+gc_status gc_testing_select_if_skip_tile0(const void *d_in, void *d_out, uint32_t *d_count,
+                                          size_t n, gc_dtype dtype, gc_pred pred, void *d_ws,
+                                          size_t ws_bytes, uint64_t timeout_ns,
+                                          cudaStream_t stream)
+{
+    if (n <= gch::select_tile_elems()) return GC_ERR_INVALID_VALUE;
+    LaunchOpts o;
+    o.timeout_ns = timeout_ns;
+    o.skip_first_tile = true;
+    return select_like(false, d_in, d_out, d_count, n, dtype, pred, d_ws, ws_bytes, stream, o);
+}
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// gc_internal.h -- host-side plumbing shared by the libgc translation units:
+// tile configurations, workspace layout arithmetic and the launchers that
+// api.cu dispatches to.  Not part of the public ABI (include/gc.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/gc.h"
+
+namespace gch {
+
+// Tile shapes: THREADS threads per CTA, ROWS 16-byte vectors per thread, so
+// a tile holds THREADS * 4 * ROWS elements.
+constexpr int kScanThreads = 256, kScanRows = 4;
+constexpr int kSelectThreads = 256, kSelectRows = 4;
+constexpr int kPartThreads = 256, kPartRows = 4;
+constexpr int kSplitThreads = 256, kSplitRows = 4;
+constexpr int kAtomicThreads = 256, kAtomicRows = 4;
+constexpr int kReduceThreads = 256;
+
+constexpr uint32_t tile_elems(int threads, int rows) { return uint32_t(threads) * 4u * uint32_t(rows); }
+
+// Workspaces are sized for the smallest tile any kernel may use, so a
+// workspace stays valid whatever tile shape a build picks.
+constexpr uint32_t kMinTileElems = 2048;
+constexpr size_t kHeaderBytes = 512;
+constexpr size_t kTileCtrOff = 504;
+
+inline size_t ceil_div(size_t a, size_t b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t a, size_t b) { return ceil_div(a, b) * b; }
+
+// Bytes of status words a call with `tiles` tiles clears and uses.
+inline size_t status_bytes(size_t tiles) { return 8 * tiles; }
+
+// Workspace capacity rules (also what gc_workspace_bytes returns).
+inline size_t max_tiles(size_t n) { return ceil_div(n, kMinTileElems) + 1; }
+inline size_t radix_temp_offset(size_t n) { return align_up(kHeaderBytes + status_bytes(max_tiles(n)), 256); }
+inline size_t radix_temp_stride(size_t n) { return align_up(4 * n, 256); }
+
+struct LaunchOpts {
+    uint64_t timeout_ns = 1000000000ull;  // a look-back wait gives up after this long
+    bool skip_first_tile = false;        // test hook: no CTA ever takes tile 0
+};
+
+// Clears the tile counter and `tiles` status words; then the kernel of the
+// call can run.  With skip_first_tile the counter starts at 1 instead.
+cudaError_t reset_tiles(uint8_t *ws, size_t tiles, cudaStream_t s, bool skip_first_tile);
+
+// Clears the header words of the count pre-pass and the radix histogram
+// (everything in the header except the error word) before those kernels.
+cudaError_t clear_accumulators(uint8_t *ws, cudaStream_t s);
+
+// Launchers.  All arguments were validated by api.cu; n >= 1.
+cudaError_t launch_scan(const void *in, void *out, void *total, uint32_t n, gc_dtype dt,
+                        uint8_t *ws, cudaStream_t s, const LaunchOpts &o);
+cudaError_t launch_select(const void *in, void *out, uint32_t *count, uint32_t n, gc_dtype dt,
+                          gc_pred p, uint8_t *ws, cudaStream_t s, const LaunchOpts &o);
+cudaError_t launch_select_atomic(const void *in, void *out, uint32_t *count, uint32_t n,
+                                 gc_dtype dt, gc_pred p, cudaStream_t s);
+cudaError_t launch_partition(const void *in, void *out, uint32_t *count_true, uint32_t n,
+                             gc_dtype dt, gc_pred p, uint8_t *ws, cudaStream_t s,
+                             const LaunchOpts &o);
+cudaError_t launch_split_radix(const uint32_t *keys_in, const uint32_t *vals_in,
+                               uint32_t *keys_out, uint32_t *vals_out, uint32_t n, int begin_bit,
+                               int end_bit, uint8_t *ws, cudaStream_t s, const LaunchOpts &o);
+
+uint32_t scan_tile_elems();
+uint32_t select_tile_elems();
+uint32_t partition_tile_elems();
+uint32_t split_tile_elems();
+uint32_t atomic_tile_elems();
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int sm_count();  // multiprocessors of the current device (cached per device)
+
+}  // namespace gch

@@ -1,0 +1,396 @@
+// partition.cu -- stable two-way partition, the one-bit split and the LSD
+// radix sort built from it.
+//
+// "compaction.cu -- Day 33" (partitionCpu, scatterPartition): rank[i], the
+// number of kept elements before i, addresses the kept half directly, and
+// i - rank[i] is the number of rejected elements before i, so one scan
+// addresses both halves; the rejected half starts at T, the total kept, which
+// must be known before anything is scattered.  T therefore comes from a count
+// pre-pass (count_kernel: one read of the input, a block reduction, one
+// atomic per CTA, and the last CTA to finish publishes the total), and the
+// main pass is the single-pass tile kernel of select.cu with two output runs
+// per tile instead of one.
+//
+// The radix sort ("CIS 565 Project 2: Stream Compaction", radix sort built
+// on scan) is that partition with the predicate "bit b clear", applied to
+// (key, payload) pairs once per bit from the lowest.  The number of keys with
+// bit b clear does not change when keys are permuted, so one histogram pass
+// over the input gives T for all 32 splits.
+#include "gc_device.cuh"
+#include "gc_internal.h"
+
+namespace {
+
+using namespace gcd;
+
+constexpr int kPad = 12;  // shared staging slack: two runs, each shifted by up to 3
+
+template <class Pred, int THREADS, int ROWS, bool VEC, bool VALS>
+__global__ void __launch_bounds__(THREADS)
+partition_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__restrict__ vals_in,
+                 uint32_t *__restrict__ keys_out, uint32_t *__restrict__ vals_out, uint32_t n,
+                 uint32_t num_tiles, const uint32_t *true_total, Pred pred, uint8_t *ws,
+                 uint64_t timeout_ns)
+{
+    using TT = Tile<THREADS, ROWS>;
+    __shared__ uint32_t s_tile;
+    __shared__ uint32_t s_chunk[TT::kChunks];
+    __shared__ uint32_t s_before, s_kept, s_total;
+    __shared__ __align__(16) uint32_t s_keys[TT::kElems + kPad];
+    __shared__ __align__(16) uint32_t s_vals[VALS ? TT::kElems + kPad : 4];
+
+    const uint32_t tile = claim_tile(ws, &s_tile);
+    if (tile >= num_tiles) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t base = tile * uint32_t(TT::kElems);
+
+    uint32_t x[ROWS][4];
+    uint32_t v[VALS ? ROWS : 1][4];
+    uint32_t mask[ROWS];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        const uint32_t idx = base + r * TT::kRowElems + 4 * tid;
+        load4<VEC>(keys_in, idx, n, 0u, x[r]);
+        if (VALS) load4<VEC>(vals_in, idx, n, 0u, v[VALS ? r : 0]);
+        uint32_t m = 0u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m |= uint32_t(idx + k < n && pred(x[r][k])) << k;
+        mask[r] = m;
+    }
+
+    uint32_t lane_excl[ROWS];
+    rank_masks<TT>(mask, lane_excl, s_chunk);
+    __syncthreads();
+
+    if (warp == 0) {
+        const uint32_t kept = scan_chunks_warp0<TT>(s_chunk);
+        uint64_t *status = reinterpret_cast<uint64_t *>(ws + kStatusOff);
+        const uint32_t before = lookback_u32(status, tile, kept, ws, timeout_ns);
+        if (lane == 0) {
+            s_before = before;
+            s_kept = kept;
+            s_total = *true_total;
+        }
+    }
+    __syncthreads();
+
+    const uint32_t before = s_before, kept = s_kept;
+    const uint32_t valid = min(uint32_t(TT::kElems), n - base);
+    const uint32_t rejected = valid - kept;
+    const uint32_t dst_kept = before;                      // rank of the tile's first kept element
+    const uint32_t dst_rej = s_total + (base - before);    // T + (i - rank[i]) at the tile start
+    // Both runs must lie inside [0, n): true only if T is the real count of
+    // kept elements.  A wrong T (a workspace corrupted between the kernels)
+    // is recorded and the stores are skipped instead of landing out of range.
+    if (uint64_t(dst_rej) + rejected > n || uint64_t(dst_kept) + kept > s_total) {
+        if (tid == 0) record_error(ws, kDeviceCheckCode, tile);
+        return;
+    }
+    const uint32_t sh_kept = VEC ? (dst_kept & 3u) : 0u;
+    const uint32_t rej_region = (sh_kept + kept + 3u) & ~3u;
+    const uint32_t sh_rej = rej_region + (VEC ? (dst_rej & 3u) : 0u);
+
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        const uint32_t local0 = r * TT::kRowElems + 4 * tid;
+        uint32_t ranked = s_chunk[r * TT::kWarps + warp] + lane_excl[r];  // kept before this item
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t local = local0 + k;
+            if (base + local < n) {
+                const uint32_t slot = ((mask[r] >> k) & 1u) ? sh_kept + ranked
+                                                            : sh_rej + (local - ranked);
+                s_keys[slot] = x[r][k];
+                if (VALS) s_vals[slot] = v[VALS ? r : 0][k];
+                ranked += (mask[r] >> k) & 1u;
+            }
+        }
+    }
+    __syncthreads();
+    store_run<THREADS, VEC>(keys_out, dst_kept, s_keys, sh_kept, kept);
+    store_run<THREADS, VEC>(keys_out, dst_rej, s_keys, sh_rej, rejected);
+    if (VALS) {
+        store_run<THREADS, VEC>(vals_out, dst_kept, s_vals, sh_kept, kept);
+        store_run<THREADS, VEC>(vals_out, dst_rej, s_vals, sh_rej, rejected);
+    }
+}
+
+// Sum of one uint32 over the CTA, returned to thread 0.
+template <int THREADS>
+__device__ __forceinline__ uint32_t block_sum(uint32_t c, uint32_t *s_warp)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    c = warp_sum(c);
+    if (lane == 0) s_warp[warp] = c;
+    __syncthreads();
+    uint32_t t = 0;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < THREADS / 32; ++w) t += s_warp[w];
+    return t;
+}
+
+// Count pre-pass of the partition: how many elements the predicate keeps.
+// Each CTA adds its count to an accumulator in the workspace header; the CTA
+// that finishes last (by a ticket counter) takes the sum, resets both words
+// for the next call, and publishes the total.
+template <class Pred, int THREADS, bool VEC>
+__global__ void __launch_bounds__(THREADS)
+count_kernel(const uint32_t *__restrict__ in, uint32_t n, Pred pred, uint8_t *ws,
+             uint32_t *count_out)
+{
+    __shared__ uint32_t s_warp[THREADS / 32];
+    constexpr uint32_t kUnroll = 4;
+    const uint32_t nvec = (n + 3u) / 4u;
+    const uint32_t stride = gridDim.x * THREADS;
+    uint32_t c = 0;
+    for (uint32_t v0 = blockIdx.x * THREADS + threadIdx.x; v0 < nvec; v0 += stride * kUnroll) {
+        uint32_t x[kUnroll][4];
+#pragma unroll
+        for (uint32_t u = 0; u < kUnroll; ++u) {
+            const uint32_t v = v0 + u * stride;
+            if (v < nvec) load4<VEC>(in, 4u * v, n, 0u, x[u]);
+        }
+#pragma unroll
+        for (uint32_t u = 0; u < kUnroll; ++u) {
+            const uint32_t v = v0 + u * stride;
+            if (v < nvec) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) c += uint32_t(4u * v + k < n && pred(x[u][k]));
+            }
+        }
+    }
+    const uint32_t total = block_sum<THREADS>(c, s_warp);
+    if (threadIdx.x == 0) {
+        atomicAdd(hdr_u32(ws, kHdrCountAcc), total);
+        __threadfence();
+        const uint32_t ticket = atomicAdd(hdr_u32(ws, kHdrReduceCtr), 1u);
+        if (ticket == gridDim.x - 1) {
+            __threadfence();
+            const uint32_t all = atomicExch(hdr_u32(ws, kHdrCountAcc), 0u);
+            atomicExch(hdr_u32(ws, kHdrReduceCtr), 0u);
+            *hdr_u32(ws, kHdrCountTrue) = all;
+            *count_out = all;
+        }
+    }
+}
+
+// Radix histogram: for every bit b, how many keys have it set.  Counted
+// eight bits at a time in byte lanes: (x >> j) & 0x01010101 holds bits j,
+// j+8, j+16, j+24 as four byte-wide 0/1 values, so eight 32-bit accumulators
+// count all 32 bits, and are spilled into 32 wide counters every 255 keys
+// before a byte can overflow.  Reduced across the warp with a butterfly
+// that leaves bit b's total in lane b, then across the CTA and the grid as in
+// count_kernel; the last CTA stores n - ones as the clear-bit count.
+template <int THREADS, bool VEC>
+__global__ void __launch_bounds__(THREADS)
+bit_histogram_kernel(const uint32_t *__restrict__ keys, uint32_t n, uint8_t *ws)
+{
+    __shared__ uint32_t s_ones[32];
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x < 32) s_ones[threadIdx.x] = 0u;
+    __syncthreads();
+
+    uint32_t ones[32];
+#pragma unroll
+    for (int b = 0; b < 32; ++b) ones[b] = 0u;
+    uint32_t acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0u;
+    uint32_t in_acc = 0;  // keys added to acc since the last spill (<= 255)
+
+    const uint32_t nvec = (n + 3u) / 4u;
+    const uint32_t stride = gridDim.x * THREADS;
+    for (uint32_t v = blockIdx.x * THREADS + threadIdx.x; v < nvec; v += stride) {
+        uint32_t x[4];
+        load4<VEC>(keys, 4u * v, n, 0u, x);  // padding keys are 0: no bits set
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] += (x[k] >> j) & 0x01010101u;
+        }
+        in_acc += 4;
+        if (in_acc > 251) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) ones[8 * q + j] += (acc[j] >> (8 * q)) & 0xffu;
+                acc[j] = 0u;
+            }
+            in_acc = 0;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ones[8 * q + j] += (acc[j] >> (8 * q)) & 0xffu;
+
+    // Butterfly reduce-scatter: after the step with offset o each lane keeps
+    // the half of its array selected by (lane & o); at the end lane l holds
+    // the warp's total for bit l in ones[0].
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+            const uint32_t send = upper ? ones[i] : ones[i + o];
+            const uint32_t keep = upper ? ones[i + o] : ones[i];
+            ones[i] = keep + __shfl_xor_sync(kFullMask, send, o);
+        }
+    }
+    atomicAdd(&s_ones[lane], ones[0]);
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        atomicAdd(hdr_u32(ws, kHdrBitAcc + 4u * threadIdx.x), s_ones[threadIdx.x]);
+        __threadfence();  // this thread's add is visible before the ticket below
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t ticket = atomicAdd(hdr_u32(ws, kHdrReduceCtr), 1u);
+        s_ones[0] = (ticket == gridDim.x - 1) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (s_ones[0] != 0u && threadIdx.x < 32) {
+        __threadfence();
+        const uint32_t total_ones = atomicExch(hdr_u32(ws, kHdrBitAcc + 4u * threadIdx.x), 0u);
+        *hdr_u32(ws, kHdrBitZeros + 4u * threadIdx.x) = n - total_ones;
+        if (threadIdx.x == 0) atomicExch(hdr_u32(ws, kHdrReduceCtr), 0u);
+    }
+}
+
+int reduce_grid(uint32_t n, int threads)
+{
+    const size_t want = gch::ceil_div(gch::ceil_div(n, 4), size_t(threads));
+    const size_t cap = size_t(gch::sm_count()) * 8;
+    return int(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+template <class Pred, bool VALS>
+cudaError_t run_partition_pass(const uint32_t *kin, const uint32_t *vin, uint32_t *kout,
+                               uint32_t *vout, uint32_t n, const uint32_t *true_total, Pred pred,
+                               uint8_t *ws, cudaStream_t s, const gch::LaunchOpts &o, bool split)
+{
+    constexpr int PT = gch::kPartThreads, PR = gch::kPartRows;
+    constexpr int ST = gch::kSplitThreads, SR = gch::kSplitRows;
+    const uint32_t tile = split ? gch::tile_elems(ST, SR) : gch::tile_elems(PT, PR);
+    const uint32_t tiles = uint32_t(gch::ceil_div(n, tile));
+    cudaError_t e = gch::reset_tiles(ws, tiles, s, o.skip_first_tile);
+    if (e != cudaSuccess) return e;
+    const uint32_t grid = o.skip_first_tile ? tiles - 1 : tiles;
+    if (grid == 0) return cudaSuccess;
+    const bool vec = gch::aligned16(kin) && gch::aligned16(kout) &&
+                     (!VALS || (gch::aligned16(vin) && gch::aligned16(vout)));
+    if (split) {
+        if (vec)
+            partition_kernel<Pred, ST, SR, true, VALS><<<grid, ST, 0, s>>>(
+                kin, vin, kout, vout, n, tiles, true_total, pred, ws, o.timeout_ns);
+        else
+            partition_kernel<Pred, ST, SR, false, VALS><<<grid, ST, 0, s>>>(
+                kin, vin, kout, vout, n, tiles, true_total, pred, ws, o.timeout_ns);
+    } else {
+        if (vec)
+            partition_kernel<Pred, PT, PR, true, VALS><<<grid, PT, 0, s>>>(
+                kin, vin, kout, vout, n, tiles, true_total, pred, ws, o.timeout_ns);
+        else
+            partition_kernel<Pred, PT, PR, false, VALS><<<grid, PT, 0, s>>>(
+                kin, vin, kout, vout, n, tiles, true_total, pred, ws, o.timeout_ns);
+    }
+    return cudaGetLastError();
+}
+
+template <class Pred>
+cudaError_t dispatch_partition(const uint32_t *in, uint32_t *out, uint32_t *count_true,
+                               uint32_t n, Pred pred, uint8_t *ws, cudaStream_t s,
+                               const gch::LaunchOpts &o)
+{
+    constexpr int RT = gch::kReduceThreads;
+    const int grid = reduce_grid(n, RT);
+    cudaError_t e0 = gch::clear_accumulators(ws, s);
+    if (e0 != cudaSuccess) return e0;
+    if (gch::aligned16(in))
+        count_kernel<Pred, RT, true><<<grid, RT, 0, s>>>(in, n, pred, ws, count_true);
+    else
+        count_kernel<Pred, RT, false><<<grid, RT, 0, s>>>(in, n, pred, ws, count_true);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const uint32_t *T = reinterpret_cast<const uint32_t *>(ws + kHdrCountTrue);
+    return run_partition_pass<Pred, false>(in, nullptr, out, nullptr, n, T, pred, ws, s, o, false);
+}
+
+}  // namespace
+
+namespace gch {
+
+uint32_t partition_tile_elems() { return tile_elems(kPartThreads, kPartRows); }
+uint32_t split_tile_elems() { return tile_elems(kSplitThreads, kSplitRows); }
+
+cudaError_t launch_partition(const void *in, void *out, uint32_t *count_true, uint32_t n,
+                             gc_dtype dt, gc_pred p, uint8_t *ws, cudaStream_t s,
+                             const LaunchOpts &o)
+{
+    auto *i = static_cast<const uint32_t *>(in);
+    auto *u = static_cast<uint32_t *>(out);
+    switch (p) {
+    case GC_PRED_NONZERO:
+        if (dt == GC_F32) return dispatch_partition(i, u, count_true, n, gcd::PredNonzeroF32{}, ws, s, o);
+        return dispatch_partition(i, u, count_true, n, gcd::PredNonzeroInt{}, ws, s, o);
+    case GC_PRED_ODD: return dispatch_partition(i, u, count_true, n, gcd::PredOdd{}, ws, s, o);
+    default: return dispatch_partition(i, u, count_true, n, gcd::PredEven{}, ws, s, o);
+    }
+}
+
+cudaError_t launch_split_radix(const uint32_t *keys_in, const uint32_t *vals_in,
+                               uint32_t *keys_out, uint32_t *vals_out, uint32_t n, int begin_bit,
+                               int end_bit, uint8_t *ws, cudaStream_t s, const LaunchOpts &o)
+{
+    const bool vals = vals_in != nullptr;
+    const int passes = end_bit - begin_bit;
+    cudaError_t e;
+    if (passes == 0) {
+        if (keys_out != keys_in) {
+            e = cudaMemcpyAsync(keys_out, keys_in, size_t(n) * 4, cudaMemcpyDeviceToDevice, s);
+            if (e != cudaSuccess) return e;
+        }
+        if (vals && vals_out != vals_in)
+            return cudaMemcpyAsync(vals_out, vals_in, size_t(n) * 4, cudaMemcpyDeviceToDevice, s);
+        return cudaSuccess;
+    }
+    constexpr int RT = kReduceThreads;
+    const int grid = reduce_grid(n, RT);
+    if ((e = clear_accumulators(ws, s)) != cudaSuccess) return e;
+    if (aligned16(keys_in))
+        bit_histogram_kernel<RT, true><<<grid, RT, 0, s>>>(keys_in, n, ws);
+    else
+        bit_histogram_kernel<RT, false><<<grid, RT, 0, s>>>(keys_in, n, ws);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+    uint32_t *tmp_k = reinterpret_cast<uint32_t *>(ws + radix_temp_offset(n));
+    uint32_t *tmp_v = reinterpret_cast<uint32_t *>(ws + radix_temp_offset(n) + radix_temp_stride(n));
+    const uint32_t *src_k = keys_in, *src_v = vals_in;
+    const bool alias = keys_in == keys_out || (vals && vals_in == vals_out);
+    if (alias && (passes & 1)) {
+        // The first split would write over its own input: start from a copy.
+        e = cudaMemcpyAsync(tmp_k, keys_in, size_t(n) * 4, cudaMemcpyDeviceToDevice, s);
+        if (e == cudaSuccess && vals)
+            e = cudaMemcpyAsync(tmp_v, vals_in, size_t(n) * 4, cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return e;
+        src_k = tmp_k;
+        src_v = vals ? tmp_v : nullptr;
+    }
+    for (int p = 0; p < passes; ++p) {
+        // The last pass writes the output; earlier ones alternate so that it does.
+        const bool to_out = ((passes - 1 - p) % 2) == 0;
+        uint32_t *dst_k = to_out ? keys_out : tmp_k;
+        uint32_t *dst_v = vals ? (to_out ? vals_out : tmp_v) : nullptr;
+        const int bit = begin_bit + p;
+        const uint32_t *T = reinterpret_cast<const uint32_t *>(ws + kHdrBitZeros + 4 * bit);
+        const gcd::PredBitClear pred{uint32_t(bit)};
+        e = vals ? run_partition_pass<gcd::PredBitClear, true>(src_k, src_v, dst_k, dst_v, n, T, pred, ws, s, o, true)
+                 : run_partition_pass<gcd::PredBitClear, false>(src_k, nullptr, dst_k, nullptr, n, T, pred, ws, s, o, true);
+        if (e != cudaSuccess) return e;
+        src_k = dst_k;
+        src_v = dst_v;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace gch

@@ -1,0 +1,194 @@
+// select.cu -- fused single-pass stable select-if, and the atomic-counter
+// comparison path.
+//
+// Stable select-if is the three steps of "compaction.cu -- Day 33" (file
+// header): predicate, exclusive scan of the 0/1 flags, scatter of survivors
+// to out[rank].  "The CUDA Handbook, ch. 13: Stream compaction" (Listing
+// 13-17) fuses them into one pass over tiles with a look-back on the tile
+// keep counts and has the highest-numbered tile write the grand total.  This
+// kernel does the same with GB300-shaped tiles:
+//   1. 128-bit loads; the predicate of each thread's 4 elements per row
+//      becomes a 4-bit mask and its popcount;
+//   2. the per-row counts (at most 128 per warp and row, so 8 bits each) are
+//      packed four to a word and scanned across the warp with shuffles: one
+//      scan yields every lane's offset in four chunks at once;
+//   3. warp 0 scans the chunk totals, publishes the tile's keep count, looks
+//      back for the number kept by all earlier tiles, publishes its own
+//      inclusive count; the last tile writes the grand total;
+//   4. survivors are placed in shared memory at their rank within the tile,
+//      shifted so that the shared and global addresses agree modulo 16 bytes,
+//      and the CTA writes its survivors as one contiguous run with 128-bit
+//      stores (scalar stores only for the partial vectors at the two ends).
+// The input is read once; only survivors and the count are written.
+#include "gc_device.cuh"
+#include "gc_internal.h"
+
+
+namespace {
+
+using namespace gcd;
+
+template <class Pred, int THREADS, int ROWS, bool VEC>
+__global__ void __launch_bounds__(THREADS)
+select_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, uint32_t *count,
+              uint32_t n, uint32_t num_tiles, Pred pred, uint8_t *ws, uint64_t timeout_ns)
+{
+    using TT = Tile<THREADS, ROWS>;
+    __shared__ uint32_t s_tile;
+    __shared__ uint32_t s_chunk[TT::kChunks];
+    __shared__ uint32_t s_base, s_kept;
+    __shared__ __align__(16) uint32_t s_buf[TT::kElems + 4];
+
+    const uint32_t tile = claim_tile(ws, &s_tile);
+    if (tile >= num_tiles) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t base = tile * uint32_t(TT::kElems);
+
+    uint32_t x[ROWS][4];
+    uint32_t mask[ROWS];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        const uint32_t idx = base + r * TT::kRowElems + 4 * tid;
+        load4<VEC>(in, idx, n, 0u, x[r]);
+        uint32_t m = 0u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m |= uint32_t(idx + k < n && pred(x[r][k])) << k;
+        mask[r] = m;
+    }
+
+    uint32_t lane_excl[ROWS];
+    rank_masks<TT>(mask, lane_excl, s_chunk);
+    __syncthreads();
+
+    if (warp == 0) {
+        const uint32_t kept = scan_chunks_warp0<TT>(s_chunk);
+        uint64_t *status = reinterpret_cast<uint64_t *>(ws + kStatusOff);
+        const uint32_t before = lookback_u32(status, tile, kept, ws, timeout_ns);
+        if (lane == 0) {
+            s_base = before;
+            s_kept = kept;
+            if (tile == num_tiles - 1) *count = before + kept;
+        }
+    }
+    __syncthreads();
+
+    const uint32_t out_base = s_base;
+    const uint32_t shift = VEC ? (out_base & 3u) : 0u;
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        uint32_t pos = shift + s_chunk[r * TT::kWarps + warp] + lane_excl[r];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if ((mask[r] >> k) & 1u) s_buf[pos++] = x[r][k];
+        }
+    }
+    __syncthreads();
+    store_run<THREADS, VEC>(out, out_base, s_buf, shift, s_kept);
+}
+
+// Comparison path ("compaction.cu -- Day 33", compactAtomic): one counter
+// for the whole grid, no scan, no order.  Survivors of one warp and row are
+// counted with a shuffle scan and claim their slots with one atomicAdd;
+// which warp reaches the counter first decides where its run lands.
+template <class Pred, int THREADS, int ROWS, bool VEC>
+__global__ void __launch_bounds__(THREADS)
+select_atomic_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out,
+                     uint32_t *count, uint32_t n, Pred pred)
+{
+    using TT = Tile<THREADS, ROWS>;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const uint32_t base = blockIdx.x * uint32_t(TT::kElems);
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        const uint32_t idx = base + r * TT::kRowElems + 4 * tid;
+        uint32_t x[4];
+        load4<VEC>(in, idx, n, 0u, x);
+        uint32_t m = 0u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m |= uint32_t(idx + k < n && pred(x[k])) << k;
+        const uint32_t c = __popc(m);
+        uint32_t incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFullMask, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const uint32_t warp_total = __shfl_sync(kFullMask, incl, 31);
+        if (warp_total == 0u) continue;
+        uint32_t slot = 0u;
+        if (lane == 31) slot = atomicAdd(count, warp_total);
+        slot = __shfl_sync(kFullMask, slot, 31) + incl - c;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if ((m >> k) & 1u) out[slot++] = x[k];
+    }
+}
+
+template <class Pred>
+cudaError_t dispatch_select(const uint32_t *in, uint32_t *out, uint32_t *count, uint32_t n,
+                            Pred pred, uint8_t *ws, cudaStream_t s, const gch::LaunchOpts &o)
+{
+    constexpr int T = gch::kSelectThreads, R = gch::kSelectRows;
+    const uint32_t tiles = uint32_t(gch::ceil_div(n, gch::tile_elems(T, R)));
+    cudaError_t e = gch::reset_tiles(ws, tiles, s, o.skip_first_tile);
+    if (e != cudaSuccess) return e;
+    const uint32_t grid = o.skip_first_tile ? tiles - 1 : tiles;
+    if (grid == 0) return cudaSuccess;
+    if (gch::aligned16(in) && gch::aligned16(out))
+        select_kernel<Pred, T, R, true><<<grid, T, 0, s>>>(in, out, count, n, tiles, pred, ws, o.timeout_ns);
+    else
+        select_kernel<Pred, T, R, false><<<grid, T, 0, s>>>(in, out, count, n, tiles, pred, ws, o.timeout_ns);
+    return cudaGetLastError();
+}
+
+template <class Pred>
+cudaError_t dispatch_atomic(const uint32_t *in, uint32_t *out, uint32_t *count, uint32_t n,
+                            Pred pred, cudaStream_t s)
+{
+    constexpr int T = gch::kAtomicThreads, R = gch::kAtomicRows;
+    const uint32_t tiles = uint32_t(gch::ceil_div(n, gch::tile_elems(T, R)));
+    cudaError_t e = cudaMemsetAsync(count, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return e;
+    if (gch::aligned16(in))
+        select_atomic_kernel<Pred, T, R, true><<<tiles, T, 0, s>>>(in, out, count, n, pred);
+    else
+        select_atomic_kernel<Pred, T, R, false><<<tiles, T, 0, s>>>(in, out, count, n, pred);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+namespace gch {
+
+uint32_t select_tile_elems() { return tile_elems(kSelectThreads, kSelectRows); }
+uint32_t atomic_tile_elems() { return tile_elems(kAtomicThreads, kAtomicRows); }
+
+cudaError_t launch_select(const void *in, void *out, uint32_t *count, uint32_t n, gc_dtype dt,
+                          gc_pred p, uint8_t *ws, cudaStream_t s, const LaunchOpts &o)
+{
+    auto *i = static_cast<const uint32_t *>(in);
+    auto *u = static_cast<uint32_t *>(out);
+    switch (p) {
+    case GC_PRED_NONZERO:
+        if (dt == GC_F32) return dispatch_select(i, u, count, n, gcd::PredNonzeroF32{}, ws, s, o);
+        return dispatch_select(i, u, count, n, gcd::PredNonzeroInt{}, ws, s, o);
+    case GC_PRED_ODD: return dispatch_select(i, u, count, n, gcd::PredOdd{}, ws, s, o);
+    default: return dispatch_select(i, u, count, n, gcd::PredEven{}, ws, s, o);
+    }
+}
+
+cudaError_t launch_select_atomic(const void *in, void *out, uint32_t *count, uint32_t n,
+                                 gc_dtype dt, gc_pred p, cudaStream_t s)
+{
+    auto *i = static_cast<const uint32_t *>(in);
+    auto *u = static_cast<uint32_t *>(out);
+    switch (p) {
+    case GC_PRED_NONZERO:
+        if (dt == GC_F32) return dispatch_atomic(i, u, count, n, gcd::PredNonzeroF32{}, s);
+        return dispatch_atomic(i, u, count, n, gcd::PredNonzeroInt{}, s);
+    case GC_PRED_ODD: return dispatch_atomic(i, u, count, n, gcd::PredOdd{}, s);
+    default: return dispatch_atomic(i, u, count, n, gcd::PredEven{}, s);
+    }
+}
+
+}  // namespace gch

@@ -1,0 +1,222 @@
+"""Python binding of libgc (include/gc.h): argument marshalling only.
+
+Every function here turns torch tensors into device pointers, sizes and enum
+codes, calls the C entry point of the same name, and raises ``GcError`` on a
+non-zero status.  No step of the computation runs in Python: the predicate,
+the scan and the scatter all run in libgc's CUDA kernels.  PyTorch supplies
+device memory and streams.
+
+The library is loaded on first use from this package's directory; if it has
+not been built (``__graft_entry__.build()`` or ``python -m
+partition_pass_tile_gb300.build``) the first call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+LIB_PATH = Path(__file__).resolve().parent / "libgc.so"
+
+# enum values of include/gc.h
+I32, U32, F32 = 0, 1, 2
+NONZERO, ODD, EVEN = 0, 1, 2
+OP_EXCLUSIVE_SCAN, OP_SELECT_IF, OP_PARTITION, OP_SPLIT_RADIX, OP_SELECT_IF_ATOMIC = range(5)
+STATUS = {0: "GC_OK", 1: "GC_ERR_INVALID_VALUE", 2: "GC_ERR_UNSUPPORTED",
+          3: "GC_ERR_WORKSPACE_TOO_SMALL", 4: "GC_ERR_MISALIGNED", 5: "GC_ERR_CUDA",
+          6: "GC_ERR_TIMEOUT", 7: "GC_ERR_DEVICE_CHECK"}
+PRED_NAMES = {"nonzero": NONZERO, "odd": ODD, "even": EVEN}
+
+_lib = None
+
+
+class GcError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+
+
+def load(path: str | Path | None = None) -> ctypes.CDLL:
+    """Load libgc.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = Path(path) if path is not None else LIB_PATH
+    if not p.exists():
+        raise RuntimeError(f"{p} is missing: build the CUDA library first "
+                           "(python -m partition_pass_tile_gb300.build)")
+    lib = ctypes.CDLL(str(p))
+    V, Z, I, U64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint64
+    S = ctypes.c_int
+    sig = {
+        "gc_status_string": ([S], ctypes.c_char_p),
+        "gc_version": ([], ctypes.c_char_p),
+        "gc_workspace_bytes": ([I, Z, I], Z),
+        "gc_tile_elements": ([I], Z),
+        "gc_workspace_init": ([V, Z, V], S),
+        "gc_exclusive_scan": ([V, V, V, Z, I, V, Z, V], S),
+        "gc_select_if": ([V, V, V, Z, I, I, V, Z, V], S),
+        "gc_partition": ([V, V, V, Z, I, I, V, Z, V], S),
+        "gc_split_radix": ([V, V, V, V, Z, I, I, V, Z, V], S),
+        "gc_select_if_atomic": ([V, V, V, Z, I, I, V, Z, V], S),
+        "gc_query_device_status": ([V, V], S),
+        "gc_testing_select_if_skip_tile0": ([V, V, V, Z, I, I, V, Z, U64, V], S),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise GcError(status, what)
+
+
+def dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.int32:
+        return I32
+    if t.dtype == torch.uint32:
+        return U32
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"libgc handles int32, uint32 and float32 tensors, not {t.dtype}")
+
+
+def pred_code(pred) -> int:
+    return PRED_NAMES[pred] if isinstance(pred, str) else int(pred)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libgc takes CUDA tensors (device pointers)")
+    if not t.is_contiguous():
+        raise ValueError("libgc takes contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def tile_elements(op: int) -> int:
+    return int(load().gc_tile_elements(op))
+
+
+def workspace_bytes(op: int, n: int, dtype: int = I32) -> int:
+    return int(load().gc_workspace_bytes(op, n, dtype))
+
+
+def workspace(op: int, n: int, dtype: int = I32, device=None) -> torch.Tensor:
+    """A zero-filled workspace for (op, n, dtype) on `device` (torch-allocated)."""
+    nbytes = max(workspace_bytes(op, n, dtype), 512)
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def _ws(ws, op, n, dtype, device):
+    return ws if ws is not None else workspace(op, n, dtype, device)
+
+
+def exclusive_scan(x: torch.Tensor, out: torch.Tensor | None = None,
+                   total: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                   stream=None, with_total: bool = True):
+    """-> (out, total); total is a 1-element device tensor of x's dtype (or None)."""
+    n = x.numel()
+    dt = dtype_code(x)
+    if out is None:
+        out = torch.empty_like(x)
+    if total is None and with_total:
+        total = torch.empty(1, dtype=x.dtype, device=x.device)
+    ws = _ws(ws, OP_EXCLUSIVE_SCAN, n, dt, x.device)
+    _check(load().gc_exclusive_scan(_ptr(x), _ptr(out), _ptr(total), n, dt, _ptr(ws),
+                                    ws.numel(), _stream(stream)), "gc_exclusive_scan")
+    return out, total
+
+
+def select_if(x: torch.Tensor, pred, out: torch.Tensor | None = None,
+              count: torch.Tensor | None = None, ws: torch.Tensor | None = None, stream=None):
+    """-> (out, count): out has x's size, its first count[0] elements are the survivors."""
+    n = x.numel()
+    dt = dtype_code(x)
+    if out is None:
+        out = torch.empty_like(x)
+    if count is None:
+        count = torch.empty(1, dtype=torch.uint32, device=x.device)
+    ws = _ws(ws, OP_SELECT_IF, n, dt, x.device)
+    _check(load().gc_select_if(_ptr(x), _ptr(out), _ptr(count), n, dt, pred_code(pred),
+                               _ptr(ws), ws.numel(), _stream(stream)), "gc_select_if")
+    return out, count
+
+
+def select_if_atomic(x: torch.Tensor, pred, out: torch.Tensor | None = None,
+                     count: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                     stream=None):
+    n = x.numel()
+    dt = dtype_code(x)
+    if out is None:
+        out = torch.empty_like(x)
+    if count is None:
+        count = torch.empty(1, dtype=torch.uint32, device=x.device)
+    ws = _ws(ws, OP_SELECT_IF_ATOMIC, n, dt, x.device)
+    _check(load().gc_select_if_atomic(_ptr(x), _ptr(out), _ptr(count), n, dt, pred_code(pred),
+                                      _ptr(ws), ws.numel(), _stream(stream)),
+           "gc_select_if_atomic")
+    return out, count
+
+
+def partition(x: torch.Tensor, pred, out: torch.Tensor | None = None,
+              count_true: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+              stream=None):
+    """-> (out, count_true)."""
+    n = x.numel()
+    dt = dtype_code(x)
+    if out is None:
+        out = torch.empty_like(x)
+    if count_true is None:
+        count_true = torch.empty(1, dtype=torch.uint32, device=x.device)
+    ws = _ws(ws, OP_PARTITION, n, dt, x.device)
+    _check(load().gc_partition(_ptr(x), _ptr(out), _ptr(count_true), n, dt, pred_code(pred),
+                               _ptr(ws), ws.numel(), _stream(stream)), "gc_partition")
+    return out, count_true
+
+
+def split_radix(keys: torch.Tensor, vals: torch.Tensor | None = None, begin_bit: int = 0,
+                end_bit: int = 32, keys_out: torch.Tensor | None = None,
+                vals_out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                stream=None):
+    """-> (keys_out, vals_out).  Keys and payloads are 32-bit (uint32 or int32 bits)."""
+    n = keys.numel()
+    for t in (keys, vals):
+        if t is not None and t.element_size() != 4:
+            raise TypeError("split_radix takes 32-bit keys and payloads")
+    if keys_out is None:
+        keys_out = torch.empty_like(keys)
+    if vals is not None and vals_out is None:
+        vals_out = torch.empty_like(vals)
+    ws = _ws(ws, OP_SPLIT_RADIX, n, U32, keys.device)
+    _check(load().gc_split_radix(_ptr(keys), _ptr(vals), _ptr(keys_out), _ptr(vals_out), n,
+                                 begin_bit, end_bit, _ptr(ws), ws.numel(), _stream(stream)),
+           "gc_split_radix")
+    return keys_out, vals_out
+
+
+def query_device_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronous: the workspace's device-side error code (0 = none), then cleared."""
+    return int(load().gc_query_device_status(_ptr(ws), _stream(stream)))
+
+
+def testing_select_if_skip_tile0(x: torch.Tensor, pred, out, count, ws, timeout_ns: int,
+                                 stream=None) -> int:
+    """Test hook (include/gc_testing.h): returns the launch status."""
+    return int(load().gc_testing_select_if_skip_tile0(
+        _ptr(x), _ptr(out), _ptr(count), x.numel(), dtype_code(x), pred_code(pred), _ptr(ws),
+        ws.numel(), timeout_ns, _stream(stream)))

@@ -1,0 +1,150 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/*.h declares, sizes workspaces, and rejects bad arguments on the host
+before any CUDA call (every call below fails validation, so nothing reaches
+the device)."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from partition_pass_tile_gb300 import build as gc_build
+from partition_pass_tile_gb300 import gc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gc_build.build()
+    return gc.load()
+
+
+def declared_functions():
+    names = set()
+    for h in ("gc.h", "gc_testing.h"):
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \t\*]*?\b(gc_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ["gc_exclusive_scan", "gc_select_if", "gc_partition", "gc_split_radix",
+                 "gc_select_if_atomic", "gc_workspace_bytes", "gc_query_device_status",
+                 "gc_status_string", "gc_workspace_init", "gc_tile_elements",
+                 "gc_testing_select_if_skip_tile0"]:
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", str(gc.LIB_PATH)], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if ln.strip()}
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = lib.gc_status_string(code)
+        assert s and s.decode().startswith(gc.STATUS[code])
+    assert lib.gc_status_string(99) == b"unknown gc_status"
+    assert b"sm_103a" in lib.gc_version()
+
+
+def test_workspace_sizes(lib):
+    for op in range(5):
+        assert lib.gc_workspace_bytes(op, 0, gc.I32) >= 512
+        assert lib.gc_workspace_bytes(op, 2 ** 31, gc.I32) == 0
+        assert lib.gc_tile_elements(op) >= 2048
+    assert lib.gc_workspace_bytes(9, 100, gc.I32) == 0
+    assert lib.gc_workspace_bytes(gc.OP_EXCLUSIVE_SCAN, 100, 7) == 0
+    # float scan keeps a double prefix per tile beside the status words
+    n = 1 << 20
+    assert lib.gc_workspace_bytes(gc.OP_EXCLUSIVE_SCAN, n, gc.F32) > \
+        lib.gc_workspace_bytes(gc.OP_EXCLUSIVE_SCAN, n, gc.I32)
+    # radix holds the ping-pong keys and payloads: at least 8 bytes per element
+    assert lib.gc_workspace_bytes(gc.OP_SPLIT_RADIX, n, gc.U32) >= 8 * n
+    # monotone in n
+    sizes = [lib.gc_workspace_bytes(gc.OP_SELECT_IF, k, gc.I32) for k in (1, 10**3, 10**6, 10**9)]
+    assert sizes == sorted(sizes)
+
+
+# Fake device addresses: never dereferenced, every call fails validation first.
+IN, OUT, CNT, WS = 0x10000000, 0x20000000, 0x30000000, 0x40000000
+BIG = 1 << 28
+
+
+def sel(lib, *, i=IN, o=OUT, c=CNT, n=1000, dt=gc.I32, p=gc.NONZERO, ws=WS, wsb=BIG,
+        fn="gc_select_if"):
+    return getattr(lib, fn)(i, o, c, n, dt, p, ws, wsb, None)
+
+
+@pytest.mark.parametrize("fn", ["gc_select_if", "gc_select_if_atomic", "gc_partition"])
+def test_select_like_validation(lib, fn):
+    E = {v: k for k, v in gc.STATUS.items()}
+    assert sel(lib, fn=fn, n=2 ** 31) == E["GC_ERR_INVALID_VALUE"]
+    assert sel(lib, fn=fn, ws=None) == E["GC_ERR_INVALID_VALUE"]
+    assert sel(lib, fn=fn, ws=WS + 16) == E["GC_ERR_MISALIGNED"]
+    assert sel(lib, fn=fn, wsb=100) == E["GC_ERR_WORKSPACE_TOO_SMALL"]
+    assert sel(lib, fn=fn, i=None) == E["GC_ERR_INVALID_VALUE"]
+    assert sel(lib, fn=fn, o=None) == E["GC_ERR_INVALID_VALUE"]
+    assert sel(lib, fn=fn, c=None) == E["GC_ERR_INVALID_VALUE"]
+    assert sel(lib, fn=fn, i=IN + 2) == E["GC_ERR_MISALIGNED"]
+    assert sel(lib, fn=fn, o=OUT + 1) == E["GC_ERR_MISALIGNED"]
+    assert sel(lib, fn=fn, c=CNT + 2) == E["GC_ERR_MISALIGNED"]
+    assert sel(lib, fn=fn, dt=gc.F32, p=gc.ODD) == E["GC_ERR_UNSUPPORTED"]
+    assert sel(lib, fn=fn, dt=gc.F32, p=gc.EVEN) == E["GC_ERR_UNSUPPORTED"]
+    assert sel(lib, fn=fn, p=7) == E["GC_ERR_INVALID_VALUE"]
+    assert sel(lib, fn=fn, dt=5) == E["GC_ERR_INVALID_VALUE"]
+    assert sel(lib, fn=fn, o=IN + 400) == E["GC_ERR_INVALID_VALUE"]        # in/out overlap
+    assert sel(lib, fn=fn, c=OUT + 40) == E["GC_ERR_INVALID_VALUE"]        # count inside out
+    assert sel(lib, fn=fn, i=WS + 4096) == E["GC_ERR_INVALID_VALUE"]       # input inside workspace
+
+
+def test_scan_validation(lib):
+    E = {v: k for k, v in gc.STATUS.items()}
+    f = lib.gc_exclusive_scan
+    assert f(IN, OUT, None, 2 ** 31, gc.I32, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+    assert f(IN, IN + 8, None, 1000, gc.I32, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]  # partial overlap
+    assert f(IN, OUT, OUT + 12, 1000, gc.I32, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]  # total in out
+    assert f(IN, OUT, CNT + 1, 1000, gc.I32, WS, BIG, None) == E["GC_ERR_MISALIGNED"]
+    assert f(IN, OUT, None, 1000, 3, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+    assert f(IN, OUT, None, 1000, gc.F32, WS, 530, None) == E["GC_ERR_WORKSPACE_TOO_SMALL"]
+    assert f(None, OUT, None, 1000, gc.I32, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+
+
+def test_radix_validation(lib):
+    E = {v: k for k, v in gc.STATUS.items()}
+    f = lib.gc_split_radix
+    K2, V1, V2 = 0x50000000, 0x60000000, 0x70000000
+    ok = dict(ki=IN, vi=V1, ko=K2, vo=V2, n=1000, b=0, e=32, ws=WS, wsb=BIG)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["ki"], a["vi"], a["ko"], a["vo"], a["n"], a["b"], a["e"], a["ws"], a["wsb"], None)
+    assert call(b=-1) == E["GC_ERR_INVALID_VALUE"]
+    assert call(e=33) == E["GC_ERR_INVALID_VALUE"]
+    assert call(b=9, e=8) == E["GC_ERR_INVALID_VALUE"]
+    assert call(vi=None) == E["GC_ERR_INVALID_VALUE"]
+    assert call(vo=None) == E["GC_ERR_INVALID_VALUE"]
+    assert call(vo=IN + 64) == E["GC_ERR_INVALID_VALUE"]       # payload over keys
+    assert call(ko=IN + 8) == E["GC_ERR_INVALID_VALUE"]        # keys partially overlap
+    assert call(vi=V1 + 2) == E["GC_ERR_MISALIGNED"]
+    assert call(wsb=1 << 12) == E["GC_ERR_WORKSPACE_TOO_SMALL"]
+    assert call(n=2 ** 31) == E["GC_ERR_INVALID_VALUE"]
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    x = torch.arange(10, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        gc.exclusive_scan(x, out=x.clone(), ws=torch.zeros(4096, dtype=torch.uint8))
+    with pytest.raises(TypeError):
+        gc.dtype_code(torch.zeros(3, dtype=torch.int64))
