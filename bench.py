@@ -1,0 +1,504 @@
+#!/usr/bin/env python3
+"""Benchmark of the predicate -> scan -> scatter hot path on one GB300 (or N, as replicas).
+
+One step runs every operation of the path over one batch of seeded synthetic
+input of n = 2^28 elements (the stable even/odd partition and selectivity
+sweep workload, 1 GiB per int32 array):
+
+    scan_i32      exclusive scan, int32 uniform random
+    scan_f32      exclusive scan, float32 uniform on [0, 1)
+    select_p01    stable select-if NONZERO, 1 % kept
+    select_p50    stable select-if NONZERO, 50 % kept
+    select_p99    stable select-if NONZERO, 99 % kept
+    partition     stable partition, EVEN first (count pre-pass + one pass)
+    radix32       LSD radix sort, 32 one-bit splits, uint32 keys + uint32 index payload
+    atomic_p50    atomic-counter select-if (the unordered comparison path), 50 % kept
+
+Every call goes through the C ABI (libgc.so) via partition_pass_tile_gb300.gc.
+Inputs are 1 GiB each, larger than the 129 MB L2, so no L2 flush is needed
+between timed steps.  Timing: W warm-up steps, then K timed steps between
+CUDA events on the launching stream, with a barrier and synchronize on both
+sides, max over ranks.  `value` counts n elements per operation and step
+(radix counts its n keys once).
+
+--impl reference times the CPU oracle (single-threaded C) on a bounded
+sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from partition_pass_tile_gb300 import synth  # noqa: E402
+
+METRIC = "compaction/scan Gelem/s and achieved HBM GB/s (% of GB300 peak) at n=2^28"
+WORKLOAD = ("stable even/odd partition + select-if sweep (1/50/99 %) at n=2^28 int32, "
+            "with exclusive scan (int32, float32), 32-bit one-bit-split LSD radix sort "
+            "(uint32 keys + index payload) and the atomic select comparator on the same batch")
+OPS = ["scan_i32", "scan_f32", "select_p01", "select_p50", "select_p99", "partition",
+       "radix32", "atomic_p50"]
+LAUNCHES_PER_OP = {"scan_i32": 1, "scan_f32": 1, "select_p01": 1, "select_p50": 1,
+                   "select_p99": 1, "partition": 2, "radix32": 33, "atomic_p50": 1}
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["gc", "reference"], default="gc")
+    p.add_argument("--n", type=int, default=1 << 28, help="elements per array (default 2^28)")
+    p.add_argument("--cpu-sample", type=int, default=1 << 24,
+                   help="elements per array in the timed CPU-oracle sample")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------- ranks
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def init_dist(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (the slowest rank sets the job's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- inputs
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Rank 0 uses the recipe's seed; replicas get their own independent batch."""
+    return seed + 1000 * rank
+
+
+def host_inputs(n: int, rank: int = 0) -> dict:
+    S = synth.SEEDS
+    x = synth.uniform_i32(n, rank_seed(S["partition"], rank))
+    return {
+        "x": x,
+        "f": synth.scan_unit_f32(n, rank_seed(S["scan_f32"], rank)),
+        "s01": synth.keep_fraction(n, 0.01, rank_seed(S["keep_0.01"], rank)),
+        "s50": synth.keep_fraction(n, 0.50, rank_seed(S["keep_0.50"], rank)),
+        "s99": synth.keep_fraction(n, 0.99, rank_seed(S["keep_0.99"], rank)),
+        "payload": np.arange(n, dtype=np.uint32),
+    }
+
+
+def alg_bytes(op: str, n: int, kept: dict) -> float:
+    """Algorithmic bytes of one call: every input element read once, every
+    output element written once (scan 8 B/elem; select 4 B + 4 B per survivor
+    + the count; partition 8 B; radix 16 B per split x 32 + a 4 B histogram
+    read; status words excluded)."""
+    if op in ("scan_i32", "scan_f32"):
+        return 8.0 * n
+    if op.startswith("select_") or op.startswith("atomic_"):
+        return 4.0 * n + 4.0 * kept[op] + 4
+    if op == "partition":
+        return 8.0 * n + 4
+    if op == "radix32":
+        return 16.0 * n * 32 + 4.0 * n
+    raise KeyError(op)
+
+
+def read_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "partition_pass_tile_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, n: int):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, scaled
+    to n elements, or None if there is none or the kernels changed since."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    return float(rec["dram_bytes_per_launch"]) * n / float(rec["n"])
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.25)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        rows = []
+        try:
+            with open(self.tmp.name) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                        rows.append(parts)
+            os.unlink(self.tmp.name)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"],
+                    "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        loaded = [s for s in sm if s >= 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": float(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())
+                if any(r[3].replace(".", "").isdigit() for r in rows) else None}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_step(orc, h: dict, n: int) -> dict:
+    """One pass of every operation of the step through the CPU oracle, on the
+    first n elements of each input.  Returns seconds per operation."""
+    import oracle as O
+    t = {}
+    x, f = h["x"][:n], h["f"][:n]
+    calls = [
+        ("scan_i32", lambda: orc.exclusive_scan(x)),
+        ("scan_f32", lambda: orc.exclusive_scan(f)),
+        ("select_p01", lambda: orc.select_if(h["s01"][:n], O.NONZERO)),
+        ("select_p50", lambda: orc.select_if(h["s50"][:n], O.NONZERO)),
+        ("select_p99", lambda: orc.select_if(h["s99"][:n], O.NONZERO)),
+        ("partition", lambda: orc.partition(x, O.EVEN)),
+        ("radix32", lambda: orc.split_radix(x.view(np.uint32), h["payload"][:n])),
+        ("atomic_p50", lambda: orc.select_if(h["s50"][:n], O.NONZERO)),
+    ]
+    for name, fn in calls:
+        t0 = time.perf_counter()
+        fn()
+        t[name] = time.perf_counter() - t0
+    return t
+
+
+def cpu_baseline(h: dict, sample: int) -> dict:
+    import oracle
+    oracle.build()
+    orc = oracle.default()
+    sample = min(sample, h["x"].shape[0])
+    t = oracle_step(orc, h, sample)
+    total = sum(t.values())
+    return {"value": len(OPS) * sample / total / 1e9, "unit": "Gelem/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"first {sample} elements of every input array, one pass of all "
+                      f"{len(OPS)} operations, single-threaded C, {total:.2f} s",
+            "ms_per_op": {k: round(v * 1e3, 3) for k, v in t.items()}}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gc(args):
+    import torch
+
+    from partition_pass_tile_gb300 import gc
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local_rank)
+    n = args.n
+    gc.load()
+
+    h = host_inputs(n, rank)
+
+    def to_dev(a):
+        t = torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else a).to(dev)
+        return t.view(torch.uint32) if a.dtype == np.uint32 else t
+
+    d = {k: to_dev(v) for k, v in h.items()}
+    out_a = torch.empty(n, dtype=torch.int32, device=dev)
+    out_b = torch.empty(n, dtype=torch.int32, device=dev)
+    counts = torch.zeros(8, dtype=torch.uint32, device=dev)
+    ws = gc.workspace(gc.OP_SPLIT_RADIX, n, gc.F32, dev)
+    assert ws.numel() >= max(gc.workspace_bytes(op, n, gc.F32) for op in range(5))
+    stream = torch.cuda.Stream(device=dev)
+    outf = out_a.view(torch.float32)
+
+    def op_calls(e2e_copy=None):
+        """The step's operations in order; e2e_copy(name) runs after each one."""
+        xk = d["x"].view(torch.uint32)
+        calls = [
+            ("scan_i32", lambda: gc.exclusive_scan(d["x"], out=out_a, total=counts[0:1].view(torch.int32), ws=ws, stream=stream)),
+            ("scan_f32", lambda: gc.exclusive_scan(d["f"], out=outf, total=counts[1:2].view(torch.float32), ws=ws, stream=stream)),
+            ("select_p01", lambda: gc.select_if(d["s01"], "nonzero", out=out_a, count=counts[2:3], ws=ws, stream=stream)),
+            ("select_p50", lambda: gc.select_if(d["s50"], "nonzero", out=out_a, count=counts[3:4], ws=ws, stream=stream)),
+            ("select_p99", lambda: gc.select_if(d["s99"], "nonzero", out=out_a, count=counts[4:5], ws=ws, stream=stream)),
+            ("partition", lambda: gc.partition(d["x"], "even", out=out_a, count_true=counts[5:6], ws=ws, stream=stream)),
+            ("radix32", lambda: gc.split_radix(xk, d["payload"], 0, 32, keys_out=out_a.view(torch.uint32),
+                                               vals_out=out_b.view(torch.uint32), ws=ws, stream=stream)),
+            ("atomic_p50", lambda: gc.select_if_atomic(d["s50"], "nonzero", out=out_a, count=counts[7:8], ws=ws, stream=stream)),
+        ]
+        return calls
+
+    def device_step(ev=None):
+        for i, (name, fn) in enumerate(op_calls()):
+            if ev is not None:
+                ev[name][0].record(stream)
+            fn()
+            if ev is not None:
+                ev[name][1].record(stream)
+
+    # warm-up (also loads every kernel)
+    for _ in range(max(args.warmup, 0)):
+        device_step()
+    stream.synchronize()
+    kept_h = counts.view(torch.int32).cpu().numpy().view(np.uint32)
+    kept = {"select_p01": int(kept_h[2]), "select_p50": int(kept_h[3]),
+            "select_p99": int(kept_h[4]), "atomic_p50": int(kept_h[7])}
+    # the counts must be the true counts of the inputs (cheap host check)
+    for k, key in (("select_p01", "s01"), ("select_p50", "s50"), ("select_p99", "s99")):
+        assert kept[k] == int(np.count_nonzero(h[key])), k
+    assert kept["atomic_p50"] == kept["select_p50"]
+    assert int(kept_h[5]) == int(np.count_nonzero((h["x"] & 1) == 0))
+
+    # timed region: every event recorded on the launching stream, read after
+    # the last step (no host synchronisation between steps)
+    def new_ev():
+        return torch.cuda.Event(enable_timing=True)
+    evs = [{name: (new_ev(), new_ev()) for name in OPS} for _ in range(args.steps)]
+    t_start, t_end = new_ev(), new_ev()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        t_start.record(stream)
+        for k in range(args.steps):
+            device_step(evs[k])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
+    ms_step = total_ms / args.steps
+    op_ms = {name: sum(e[name][0].elapsed_time(e[name][1]) for e in evs) / args.steps
+             for name in OPS}
+
+    # end to end: pinned host inputs in, outputs and counts back, every step
+    pinned = {k: torch.from_numpy(v.view(np.int32) if v.dtype == np.uint32 else v).pin_memory()
+              for k, v in h.items()}
+    host_out = torch.empty(n, dtype=torch.int32).pin_memory()
+    host_out_b = torch.empty(n, dtype=torch.int32).pin_memory()
+    host_counts = torch.empty(8, dtype=torch.int32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h_per_op = {"radix32": 2 * 4 * n}
+    d2h = sum(d2h_per_op.get(k, 4 * n) for k in OPS) + host_counts.numel() * 4
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for k, v in pinned.items():
+                dst = d[k].view(torch.int32) if d[k].dtype == torch.uint32 else d[k]
+                dst.copy_(v, non_blocking=True)
+            for name, fn in op_calls():
+                fn()
+                host_out.copy_(out_a, non_blocking=True)
+                if name == "radix32":
+                    host_out_b.copy_(out_b, non_blocking=True)
+            host_counts.copy_(counts.view(torch.int32), non_blocking=True)
+
+    e2e_step()
+    stream.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
+
+    peak, peak_kind = read_peaks()
+    elems_step = len(OPS) * n
+    bytes_step = sum(alg_bytes(k, n, kept) for k in OPS)
+    ops_report = {}
+    for k in OPS:
+        b = alg_bytes(k, n, kept)
+        ops_report[k] = {"ms": round(op_ms[k], 4), "gelem_s": round(n / op_ms[k] / 1e6, 2),
+                         "alg_gbs": round(b / op_ms[k] / 1e6, 1),
+                         "frac_of_peak": round(b / op_ms[k] / 1e6 / peak, 4),
+                         "launches": LAUNCHES_PER_OP[k]}
+    # dominant kernel: the one-bit split of the radix sort (32 launches per sort)
+    split_bytes = 16.0 * n
+    split_ms = op_ms["radix32"] / 32.0
+    achieved = split_bytes / split_ms / 1e6
+    result = {
+        "metric": METRIC,
+        "value": round(sum_over_ranks(elems_step, world, dev) / (ms_step / 1e3) / 1e9, 3),
+        "unit": "Gelem/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int32/uint32/f32",
+        "data": "synthetic (seeded SplitMix64)",
+        "config": {"workload": WORKLOAD, "n": n, "bytes_per_array": 4 * n,
+                   "ops_per_step": OPS, "elements_per_step": elems_step,
+                   "alg_bytes_per_step": bytes_step,
+                   "alg_gbs": round(bytes_step / ms_step / 1e6, 1),
+                   "frac_of_hbm_peak": round(bytes_step / ms_step / 1e6 / peak, 4),
+                   "l2": "inputs 1 GiB each, larger than L2: no flush between steps",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "ops": ops_report,
+        "roofline": {"kernel": "partition_kernel<PredBitClear, payload> (one-bit radix split)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} hbm_gbs",
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic("split_kernel", n),
+                     "alg_bytes_per_launch": split_bytes,
+                     "duration_note": "radix32 call time / 32: includes the histogram pass "
+                                      "and each split's status-word clear"},
+        "clocks": clocks.summary(),
+        "e2e": {"value": round(sum_over_ranks(elems_step, world, dev) / (e2e_ms / 1e3) / 1e9, 3),
+                "unit": "Gelem/s", "ms_per_step": round(e2e_ms, 3),
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "path": "pinned host buffers -> H2D -> gc_* through the C ABI -> D2H of every output"},
+        "gpu_launches": sum(LAUNCHES_PER_OP.values()) * args.steps,
+    }
+    if rank == 0:
+        if world == 1:
+            result["cpu_baseline"] = cpu_baseline(h, args.cpu_sample)
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    orc = oracle.default()
+    sample = min(args.cpu_sample >> 2, args.n)
+    h = host_inputs(sample, 0)
+    for _ in range(max(args.warmup, 0)):
+        oracle_step(orc, h, sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(orc, h, sample)
+    sec = (time.perf_counter() - t0) / max(args.steps, 1)
+    value = len(OPS) * sample / sec / 1e9
+    result = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "Gelem/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int32/uint32/f64", "data": "synthetic (seeded SplitMix64)",
+        "config": {"workload": WORKLOAD, "n": args.n, "sample_n": sample,
+                   "ops_per_step": OPS, "parallelism": "host CPU, one core"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "Gelem/s", "kind": "oracle",
+                         "cores": 1,
+                         "sample": f"each step: the first {sample} elements of every input "
+                                   f"array of the n={args.n} workload, all {len(OPS)} "
+                                   "operations, single-threaded C oracle"},
+        "e2e": {"value": round(value, 4), "unit": "Gelem/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(result), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gc(args)
+
+
+if __name__ == "__main__":
+    main()
