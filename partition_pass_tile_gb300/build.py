@@ -44,8 +44,12 @@ def _stale(out: Path, deps: list[Path]) -> bool:
     return any(d.stat().st_mtime > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> Path:
-    """Compile and link libgc.so next to this file; returns its path."""
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          lib: Path | None = None, build_dir: Path | None = None) -> Path:
+    """Compile and link libgc.so (next to this file unless `lib` names another
+    path, e.g. a variant built with different -D tile sizes); returns its path."""
+    LIB = Path(lib) if lib is not None else globals()["LIB"]
+    BUILD_DIR = Path(build_dir) if build_dir is not None else globals()["BUILD_DIR"]
     BUILD_DIR.mkdir(parents=True, exist_ok=True)
     headers = sorted(CSRC.glob("*.cuh")) + sorted(CSRC.glob("*.h")) + sorted(INCLUDE.glob("*.h"))
     flags = NVCC_FLAGS + list(extra_flags or [])

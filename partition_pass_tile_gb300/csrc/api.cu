@@ -40,6 +40,20 @@ int sm_count()
     return cached[dev];
 }
 
+int persistent_grid(const void *kernel, int threads, size_t smem, uint32_t tiles)
+{
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+        cudaSuccess)
+        return -1;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) !=
+            cudaSuccess ||
+        per_sm <= 0)
+        return -1;
+    const long long grid = (long long)per_sm * sm_count();
+    return int(grid < (long long)tiles ? grid : (long long)tiles);
+}
+
 }  // namespace gch
 
 namespace {

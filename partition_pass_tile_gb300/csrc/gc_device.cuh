@@ -428,4 +428,355 @@ __device__ __forceinline__ void rank_masks(const uint32_t (&mask)[TT::kRows],
     }
 }
 
+// ---------------------------------------------------------------- CTA-wide look-back
+//
+// The same look-back with every thread of the CTA reading one predecessor, so
+// one window covers THREADS tiles instead of 32.  Warps summarise their part
+// of the window (is there a prefix, is anything missing before it, the sum up
+// to it) in shared memory, and every thread combines the summaries in warp
+// order, closest warp first.  The summaries are double-buffered by iteration
+// parity, so one barrier per window suffices.  The time limit is decided from
+// the warp leaders' clocks, OR-ed through the same summaries, so the whole
+// CTA gives up in the same iteration.
+struct LookbackSmem {
+    uint32_t info[2][32];  // bit 0: prefix seen, bit 1: missing before it, bit 2: time is up
+    uint32_t sum_u32[2][32];
+    double sum_f64[2][32];
+};
+
+template <int THREADS, bool F32>
+__device__ __forceinline__ void lookback_cta_impl(uint64_t *status, const double *prefix64,
+                                                  uint32_t tile, uint8_t *ws, uint64_t timeout_ns,
+                                                  LookbackSmem &sm, uint32_t &ex_u32,
+                                                  double &ex_f64)
+{
+    constexpr int W = THREADS / 32;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    int64_t win = int64_t(tile) - 1;
+    int parity = 0;
+    uint32_t spins = 0;
+    uint64_t t_start = 0;
+    ex_u32 = 0u;
+    ex_f64 = 0.0;
+    for (;;) {
+        const int64_t j = win - t;
+        uint32_t value = 0u, flag = kFlagPrefix;
+        if (j >= 0) {
+            const uint64_t w = ld_relaxed_gpu(status + j);
+            value = uint32_t(w);
+            flag = uint32_t(w >> 32);
+        }
+        const uint32_t pm = __ballot_sync(kFullMask, flag == kFlagPrefix);
+        const uint32_t xm = __ballot_sync(kFullMask, flag == kFlagNone);
+        const uint32_t use = lanes_up_to_first(pm);
+        const bool mine = (use >> lane) & 1u;
+        uint32_t su = 0u;
+        double sd = 0.0;
+        if (F32) {
+            if (mine) {
+                if (flag == kFlagPrefix && j >= 0) {
+                    __threadfence();
+                    sd = ld_relaxed_gpu_f64(prefix64 + j);
+                } else if (flag == kFlagAggregate) {
+                    sd = double(__uint_as_float(value));
+                }
+            }
+            sd = warp_sum(sd);
+        } else {
+            su = warp_sum(mine && flag != kFlagNone ? value : 0u);
+        }
+        if (lane == 0) {
+            const bool expired = spins > 0 && global_timer_ns() - t_start > timeout_ns;
+            sm.info[parity][warp] = uint32_t(pm != 0u) | (uint32_t((xm & use) != 0u) << 1) |
+                                    (uint32_t(expired) << 2);
+            if (F32) sm.sum_f64[parity][warp] = sd; else sm.sum_u32[parity][warp] = su;
+        }
+        __syncthreads();
+        uint32_t acc_u = 0u;
+        double acc_d = 0.0;
+        bool found = false, missing = false, expired = false;
+#pragma unroll 1
+        for (int w = 0; w < W; ++w) {
+            const uint32_t info = sm.info[parity][w];
+            expired |= (info >> 2) & 1u;
+            if (!found) {
+                missing |= (info >> 1) & 1u;
+                if (F32) acc_d += sm.sum_f64[parity][w]; else acc_u += sm.sum_u32[parity][w];
+                found = info & 1u;
+            }
+        }
+        parity ^= 1;
+        if (!missing || expired) {
+            if (missing && t == 0) record_error(ws, kTimeoutCode, tile);
+            ex_u32 += acc_u;
+            ex_f64 += acc_d;
+            if (found || missing) return;  // a prefix ends the walk; so does the time limit
+            win -= THREADS;
+            spins = 0;
+            continue;
+        }
+        if (spins == 0) t_start = global_timer_ns();
+        ++spins;
+        __nanosleep(spins < 8 ? 20 : 100);
+    }
+}
+
+// The tile's exclusive prefix and total, to every thread of the CTA.
+// Chunk totals are in s_chunk (warp 0 scans them into offsets); warp 0 lane 0
+// publishes the aggregate (or, for tile 0, the prefix) and, after the
+// look-back, the inclusive prefix.  CTA_LOOKBACK picks the CTA-wide walk,
+// otherwise warp 0 walks alone while the other warps wait at the barrier.
+struct PrefixSmem {
+    LookbackSmem lb;
+    uint32_t res_u32[2];
+    double res_f64;
+    float agg_f32;
+};
+
+template <class TT, bool CTA_LOOKBACK>
+__device__ __forceinline__ void resolve_prefix_u32(uint32_t *s_chunk, uint32_t tile, uint8_t *ws,
+                                                   uint64_t timeout_ns, PrefixSmem &ps,
+                                                   uint32_t &prefix, uint32_t &total)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t *status = reinterpret_cast<uint64_t *>(ws + kStatusOff);
+    if (!CTA_LOOKBACK) {
+        if (warp == 0) {
+            const uint32_t agg = scan_chunks_warp0<TT>(s_chunk);
+            const uint32_t ex = lookback_u32(status, tile, agg, ws, timeout_ns);
+            if (lane == 0) {
+                ps.res_u32[0] = ex;
+                ps.res_u32[1] = agg;
+            }
+        }
+        __syncthreads();
+        prefix = ps.res_u32[0];
+        total = ps.res_u32[1];
+        return;
+    }
+    if (warp == 0) {
+        const uint32_t agg = scan_chunks_warp0<TT>(s_chunk);
+        if (lane == 0) {
+            ps.res_u32[1] = agg;
+            st_relaxed_gpu(status + tile, pack_status(agg, tile == 0 ? kFlagPrefix : kFlagAggregate));
+        }
+    }
+    __syncthreads();
+    total = ps.res_u32[1];
+    prefix = 0u;
+    if (tile != 0) {
+        double unused;
+        lookback_cta_impl<TT::kThreads, false>(status, nullptr, tile, ws, timeout_ns, ps.lb, prefix,
+                                               unused);
+        if (threadIdx.x == 0) st_relaxed_gpu(status + tile, pack_status(prefix + total, kFlagPrefix));
+    }
+}
+
+template <class TT, bool CTA_LOOKBACK>
+__device__ __forceinline__ void resolve_prefix_f32(float *s_chunk, uint32_t tile, uint8_t *ws,
+                                                   double *prefix64, uint64_t timeout_ns,
+                                                   PrefixSmem &ps, double &prefix, float &total)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t *status = reinterpret_cast<uint64_t *>(ws + kStatusOff);
+    if (!CTA_LOOKBACK) {
+        if (warp == 0) {
+            const float agg = scan_chunks_warp0<TT>(s_chunk);
+            const double ex = lookback_f32(status, prefix64, tile, agg, ws, timeout_ns);
+            if (lane == 0) {
+                ps.res_f64 = ex;
+                ps.agg_f32 = agg;
+            }
+        }
+        __syncthreads();
+        prefix = ps.res_f64;
+        total = ps.agg_f32;
+        return;
+    }
+    if (warp == 0) {
+        const float agg = scan_chunks_warp0<TT>(s_chunk);
+        if (lane == 0) {
+            ps.agg_f32 = agg;
+            if (tile == 0) {
+                st_relaxed_gpu_f64(prefix64, double(agg));
+                st_release_gpu(status, pack_status(__float_as_uint(agg), kFlagPrefix));
+            } else {
+                st_relaxed_gpu(status + tile, pack_status(__float_as_uint(agg), kFlagAggregate));
+            }
+        }
+    }
+    __syncthreads();
+    total = ps.agg_f32;
+    prefix = 0.0;
+    if (tile != 0) {
+        uint32_t unused;
+        lookback_cta_impl<TT::kThreads, true>(status, prefix64, tile, ws, timeout_ns, ps.lb, unused,
+                                              prefix);
+        if (threadIdx.x == 0) {
+            const double inclusive = prefix + double(total);
+            st_relaxed_gpu_f64(prefix64 + tile, inclusive);
+            st_release_gpu(status + tile, pack_status(__float_as_uint(float(inclusive)), kFlagPrefix));
+        }
+    }
+}
+
+// ---------------------------------------------------------------- fixed-window prefix
+//
+// The persistent kernels own tiles round-robin: CTA c of G takes tiles c,
+// c + G, c + 2G, ...  Each CTA keeps the inclusive prefix of its previous
+// tile, R (the sum of every tile up to and including tile k - G), so the
+// exclusive prefix of tile k is
+//
+//     prefix(k) = R + agg(k - G + 1) + ... + agg(k - 1)
+//
+// (for k < G: agg(0) + ... + agg(k - 1)).  Those G - 1 aggregates are
+// published by the other CTAs as soon as they have reduced their tile, before
+// they wait on anything, so one CTA-wide read of at most G - 1 status words
+// gives the prefix: no tile ever waits on another tile's look-back, only on
+// its aggregate.  This is the decoupled look-back of the CUDA Handbook's
+// single-pass scan with the walk ending, always, at the CTA's own previous
+// tile, whose inclusive prefix the CTA already holds.
+
+// Publishes a tile's aggregate (one 64-bit store: value and flag together).
+__device__ __forceinline__ void publish_aggregate(uint64_t *status, uint32_t tile, uint32_t bits)
+{
+    st_relaxed_gpu(status + tile, pack_status(bits, kFlagAggregate));
+}
+
+// Reads status word j until its aggregate is published (bounded wait: past
+// timeout_ns it records GC_ERR_TIMEOUT and returns 0 for it).
+__device__ __forceinline__ uint32_t await_aggregate(const uint64_t *status, uint32_t j, uint8_t *ws,
+                                                    uint32_t tile, uint64_t timeout_ns)
+{
+    uint64_t w = ld_relaxed_gpu(status + j);
+    if (uint32_t(w >> 32) != kFlagNone) return uint32_t(w);
+    const uint64_t t0 = global_timer_ns();
+    uint32_t spins = 0;
+    for (;;) {
+        __nanosleep(spins < 8 ? 32 : 128);
+        ++spins;
+        w = ld_relaxed_gpu(status + j);
+        if (uint32_t(w >> 32) != kFlagNone) return uint32_t(w);
+        if (global_timer_ns() - t0 > timeout_ns) {
+            record_error(ws, kTimeoutCode, tile);
+            return 0u;
+        }
+    }
+}
+
+// Sum over the aggregates of tiles [lo, hi), read by all THREADS threads and
+// reduced across the CTA (uint32 wrap-around, or float32 aggregates summed in
+// double).  Every thread gets the sum.  s_red: THREADS / 32 slots.
+template <int THREADS>
+__device__ __forceinline__ uint32_t window_sum_u32(const uint64_t *status, uint32_t lo, uint32_t hi,
+                                                   uint8_t *ws, uint32_t tile,
+                                                   uint64_t timeout_ns, uint32_t *s_red)
+{
+    uint32_t sum = 0u;
+    for (uint32_t j = lo + threadIdx.x; j < hi; j += THREADS)
+        sum += await_aggregate(status, j, ws, tile, timeout_ns);
+    sum = warp_sum(sum);
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = sum;
+    __syncthreads();
+    uint32_t total = 0u;
+#pragma unroll
+    for (int w = 0; w < THREADS / 32; ++w) total += s_red[w];
+    return total;
+}
+
+template <int THREADS>
+__device__ __forceinline__ double window_sum_f32(const uint64_t *status, uint32_t lo, uint32_t hi,
+                                                 uint8_t *ws, uint32_t tile, uint64_t timeout_ns,
+                                                 double *s_red)
+{
+    double sum = 0.0;
+    for (uint32_t j = lo + threadIdx.x; j < hi; j += THREADS)
+        sum += double(__uint_as_float(await_aggregate(status, j, ws, tile, timeout_ns)));
+    sum = warp_sum(sum);
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = sum;
+    __syncthreads();
+    double total = 0.0;
+#pragma unroll
+    for (int w = 0; w < THREADS / 32; ++w) total += s_red[w];
+    return total;
+}
+
+// First tile of the window of tile k (the tiles after this CTA's previous one).
+__device__ __forceinline__ uint32_t window_lo(uint32_t k)
+{
+    return k >= gridDim.x ? k - gridDim.x + 1u : 0u;
+}
+
+// ---------------------------------------------------------------- lagged window
+//
+// The window of a tile is read one iteration after its aggregates were
+// published: a CTA reduces and publishes tile k, then finishes tile k - G
+// (its previous one), whose window [k - 2G + 1, k - G) every CTA published a
+// whole iteration earlier.  The loads of that window are issued before the
+// reduction of tile k and consumed after it, so their latency overlaps the
+// reduction.  kWinPerThread bounds the window: G - 1 <= THREADS * kWinPerThread.
+constexpr int kWinPerThread = 4;
+
+struct WindowLoads {
+    uint64_t w[kWinPerThread];
+};
+
+template <int THREADS>
+__device__ __forceinline__ void window_issue(const uint64_t *status, uint32_t lo, uint32_t hi,
+                                             WindowLoads &wl)
+{
+#pragma unroll
+    for (int i = 0; i < kWinPerThread; ++i) {
+        const uint32_t j = lo + threadIdx.x + uint32_t(i) * THREADS;
+        wl.w[i] = j < hi ? ld_relaxed_gpu(status + j) : pack_status(0u, kFlagAggregate);
+    }
+}
+
+// Completes the loads of window_issue (re-reading any word not yet
+// published, bounded) and reduces them over the CTA; every thread gets the
+// sum.  F32: the words hold float32 aggregates, summed in double.
+template <int THREADS, bool F32>
+__device__ __forceinline__ void window_finish(const uint64_t *status, uint32_t lo, uint32_t hi,
+                                              WindowLoads &wl, uint8_t *ws, uint32_t tile,
+                                              uint64_t timeout_ns, uint32_t *s_red_u,
+                                              double *s_red_d, uint32_t &sum_u, double &sum_d)
+{
+    uint32_t su = 0u;
+    double sd = 0.0;
+#pragma unroll
+    for (int i = 0; i < kWinPerThread; ++i) {
+        const uint32_t j = lo + threadIdx.x + uint32_t(i) * THREADS;
+        uint32_t v = uint32_t(wl.w[i]);
+        if (j < hi && uint32_t(wl.w[i] >> 32) == kFlagNone) v = await_aggregate(status, j, ws, tile, timeout_ns);
+        if (F32) sd += double(__uint_as_float(v)); else su += v;
+    }
+    if (F32) {
+        sd = warp_sum(sd);
+        if ((threadIdx.x & 31) == 0) s_red_d[threadIdx.x >> 5] = sd;
+    } else {
+        su = warp_sum(su);
+        if ((threadIdx.x & 31) == 0) s_red_u[threadIdx.x >> 5] = su;
+    }
+    __syncthreads();
+    sum_u = 0u;
+    sum_d = 0.0;
+#pragma unroll
+    for (int w = 0; w < THREADS / 32; ++w) {
+        if (F32) sum_d += s_red_d[w]; else sum_u += s_red_u[w];
+    }
+}
+
+// Sum of one value over the CTA, to every thread.
+template <int THREADS, class V>
+__device__ __forceinline__ V block_sum_all(V v, V *s_red)
+{
+    v = warp_sum(v);
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    V t = V(0);
+#pragma unroll
+    for (int w = 0; w < THREADS / 32; ++w) t += s_red[w];
+    return t;
+}
+
 }  // namespace gcd

@@ -13,13 +13,91 @@
 namespace gch {
 
 // Tile shapes: THREADS threads per CTA, ROWS 16-byte vectors per thread, so
-// a tile holds THREADS * 4 * ROWS elements.
-constexpr int kScanThreads = 256, kScanRows = 4;
-constexpr int kSelectThreads = 256, kSelectRows = 4;
-constexpr int kPartThreads = 256, kPartRows = 4;
-constexpr int kSplitThreads = 256, kSplitRows = 4;
+// a tile holds THREADS * 4 * ROWS elements.  Overridable at build time
+// (-DGC_SCAN_ROWS=8 ...) for tuning sweeps.
+#ifndef GC_SCAN_THREADS
+#define GC_SCAN_THREADS 256
+#endif
+#ifndef GC_SCAN_ROWS
+#define GC_SCAN_ROWS 4
+#endif
+#ifndef GC_SELECT_THREADS
+#define GC_SELECT_THREADS 256
+#endif
+#ifndef GC_SELECT_ROWS
+#define GC_SELECT_ROWS 4
+#endif
+#ifndef GC_PART_THREADS
+#define GC_PART_THREADS 256
+#endif
+#ifndef GC_PART_ROWS
+#define GC_PART_ROWS 4
+#endif
+#ifndef GC_SPLIT_THREADS
+#define GC_SPLIT_THREADS 256
+#endif
+#ifndef GC_SPLIT_ROWS
+#define GC_SPLIT_ROWS 4
+#endif
+// 1: every thread of the CTA takes part in the look-back (THREADS tiles per
+// window); 0: warp 0 alone (32 tiles per window).
+#ifndef GC_CTA_LOOKBACK
+#define GC_CTA_LOOKBACK 0
+#endif
+// Persistent pipelined kernels: tile shape and the number of tiles in flight
+// per CTA (each stage is one tile buffer in shared memory).
+#ifndef GC_SCAN_PIPE_THREADS
+#define GC_SCAN_PIPE_THREADS 256
+#endif
+#ifndef GC_SCAN_PIPE_ROWS
+#define GC_SCAN_PIPE_ROWS 8
+#endif
+#ifndef GC_SCAN_PIPE_STAGES
+#define GC_SCAN_PIPE_STAGES 3
+#endif
+constexpr int kScanPipeThreads = GC_SCAN_PIPE_THREADS, kScanPipeRows = GC_SCAN_PIPE_ROWS;
+constexpr int kScanPipeStages = GC_SCAN_PIPE_STAGES;
+#ifndef GC_SELECT_PIPE_THREADS
+#define GC_SELECT_PIPE_THREADS 256
+#endif
+#ifndef GC_SELECT_PIPE_ROWS
+#define GC_SELECT_PIPE_ROWS 8
+#endif
+#ifndef GC_SELECT_PIPE_STAGES
+#define GC_SELECT_PIPE_STAGES 3
+#endif
+#ifndef GC_PART_PIPE_THREADS
+#define GC_PART_PIPE_THREADS 256
+#endif
+#ifndef GC_PART_PIPE_ROWS
+#define GC_PART_PIPE_ROWS 8
+#endif
+#ifndef GC_PART_PIPE_STAGES
+#define GC_PART_PIPE_STAGES 3
+#endif
+#ifndef GC_SPLIT_PIPE_THREADS
+#define GC_SPLIT_PIPE_THREADS 256
+#endif
+#ifndef GC_SPLIT_PIPE_ROWS
+#define GC_SPLIT_PIPE_ROWS 4
+#endif
+#ifndef GC_SPLIT_PIPE_STAGES
+#define GC_SPLIT_PIPE_STAGES 3
+#endif
+constexpr int kSelectPipeThreads = GC_SELECT_PIPE_THREADS, kSelectPipeRows = GC_SELECT_PIPE_ROWS;
+constexpr int kSelectPipeStages = GC_SELECT_PIPE_STAGES;
+constexpr int kPartPipeThreads = GC_PART_PIPE_THREADS, kPartPipeRows = GC_PART_PIPE_ROWS;
+constexpr int kPartPipeStages = GC_PART_PIPE_STAGES;
+constexpr int kSplitPipeThreads = GC_SPLIT_PIPE_THREADS, kSplitPipeRows = GC_SPLIT_PIPE_ROWS;
+constexpr int kSplitPipeStages = GC_SPLIT_PIPE_STAGES;
+
+constexpr int kScanThreads = GC_SCAN_THREADS, kScanRows = GC_SCAN_ROWS;
+constexpr int kSelectThreads = GC_SELECT_THREADS, kSelectRows = GC_SELECT_ROWS;
+constexpr int kPartThreads = GC_PART_THREADS, kPartRows = GC_PART_ROWS;
+constexpr int kSplitThreads = GC_SPLIT_THREADS, kSplitRows = GC_SPLIT_ROWS;
 constexpr int kAtomicThreads = 256, kAtomicRows = 4;
 constexpr int kReduceThreads = 256;
+constexpr bool kCtaLookback = GC_CTA_LOOKBACK != 0;
 
 constexpr uint32_t tile_elems(int threads, int rows) { return uint32_t(threads) * 4u * uint32_t(rows); }
 
@@ -76,5 +154,10 @@ uint32_t atomic_tile_elems();
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int sm_count();  // multiprocessors of the current device (cached per device)
+
+// Grid of a persistent kernel: as many CTAs as fit on the device at once
+// (never more than there are tiles).  Raises the kernel's dynamic shared
+// memory limit to `smem` first.  Returns <= 0 on failure.
+int persistent_grid(const void *kernel, int threads, size_t smem, uint32_t tiles);
 
 }  // namespace gch

@@ -1,0 +1,42 @@
+// gc_launch.cuh -- host side of the persistent pipelined kernels: one
+// __global__ wrapper around pipeline_run and its cooperative launch.
+#pragma once
+
+#include <algorithm>
+
+#include "gc_internal.h"
+#include "gc_tiles.cuh"
+
+namespace gcd {
+
+template <int THREADS, int STAGES, class Op>
+__global__ void __launch_bounds__(THREADS)
+pipeline_kernel(Op op, uint32_t n, uint32_t num_tiles, uint8_t *ws, uint64_t timeout_ns)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    pipeline_run<THREADS, STAGES>(op, smem, n, num_tiles, ws, timeout_ns);
+}
+
+// Clears this call's tile status words and launches the cooperative
+// persistent grid (as many CTAs as fit, at most one per tile).  Returns the
+// launch error; a refused cooperative launch (the device cannot hold the
+// grid right now) lets the caller fall back to a one-tile-per-CTA kernel.
+template <int THREADS, int STAGES, class Op>
+cudaError_t launch_pipeline(const Op &op, uint32_t n, uint8_t *ws, cudaStream_t s,
+                            uint64_t timeout_ns)
+{
+    uint32_t tiles = uint32_t(gch::ceil_div(n, Op::kTileElems));
+    cudaError_t e = gch::reset_tiles(ws, tiles, s, false);
+    if (e != cudaSuccess) return e;
+    auto kernel = pipeline_kernel<THREADS, STAGES, Op>;
+    constexpr uint32_t smem = Op::template PipeT<STAGES>::kBytes;
+    int grid = gch::persistent_grid(reinterpret_cast<const void *>(kernel), THREADS, smem, tiles);
+    if (grid <= 0) return cudaErrorInvalidConfiguration;
+    grid = std::min(grid, pipeline_max_grid<THREADS>());
+    Op op_copy = op;
+    void *args[] = {&op_copy, &n, &tiles, &ws, &timeout_ns};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kernel), dim3(grid),
+                                       dim3(THREADS), args, smem, s);
+}
+
+}  // namespace gcd

@@ -1,0 +1,201 @@
+// gc_pipe.cuh -- the load pipeline of the persistent tile kernels: tiles are
+// copied from global into shared memory by the TMA unit (cp.async.bulk, one
+// bulk copy per tile, completion signalled on an mbarrier), STAGES tiles
+// ahead of the tile being computed on.
+//
+// Why: a tile kernel spends part of every tile waiting for its look-back
+// (the predecessors' prefixes), and while it waits it issues no loads.  With
+// the next STAGES - 1 tiles already in flight into shared memory the memory
+// system stays busy through that wait, so the kernel can stream at the HBM
+// rate with one or two CTAs per SM.
+//
+// Schedule: the grid is launched cooperatively (every CTA resident at once)
+// and CTA c owns tiles c, c + G, c + 2G, ... (G = gridDim.x), which it
+// computes in that order and prefetches STAGES ahead.  Tile k's look-back
+// waits only on tiles below k, each owned by a resident CTA that reaches it
+// before any later tile of its own, so the smallest unfinished tile is always
+// being worked on: the look-back always makes progress.  Prefetching only a
+// CTA's own future tiles keeps every claimed tile close to being published;
+// tiles taken from a shared counter ahead of time would sit unpublished in
+// one CTA's queue and stall every later tile's look-back.
+//
+// Protocol, per stage s (one mbarrier each, arrival count 1): thread 0 does
+// arrive.expect_tx(bytes) and issues the bulk copy of the tile's first
+// `bytes` bytes (the largest multiple of 16 the tile holds; the ragged tail
+// of the last tile is read with plain loads by the consumers); all threads
+// wait on the stage's phase parity, compute, and after a barrier thread 0
+// re-arms the stage with the CTA's tile STAGES rounds later.
+#pragma once
+
+#include <cstdint>
+
+#include "gc_device.cuh"
+
+namespace gcd {
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0u;
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from global src (16-byte aligned)
+// into shared dst (16-byte aligned); completion is counted on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Waits for a stage's phase.  The wait is bounded: past timeout_ns of device
+// time it records GC_ERR_TIMEOUT and returns, and the caller carries on with
+// whatever the buffer holds (every thread follows the same path afterwards,
+// so no barrier is ever left unmatched).
+__device__ __forceinline__ void mbar_wait(uint64_t *bar, uint32_t parity, uint8_t *ws,
+                                          uint64_t timeout_ns)
+{
+    if (mbar_try_wait(bar, parity)) return;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > timeout_ns) {
+            record_error(ws, kTimeoutCode, 0xffffffffu);
+            return;
+        }
+    }
+}
+
+// Shared-memory layout of a pipelined kernel: STAGES stages, each holding one
+// tile buffer per input array (ARRAYS of them: keys and payloads for the
+// radix split), then the mbarriers.  Every buffer has 128 bytes of slack
+// after the tile, room for the in-place compaction of select-if and
+// partition, whose runs are shifted by up to 3 (each) elements to line up
+// with 16-byte global addresses.
+template <uint32_t TILE_BYTES, int STAGES, int ARRAYS = 1>
+struct Pipe {
+    static constexpr uint32_t kArrBytes = TILE_BYTES + 128u;
+    static constexpr uint32_t kStageBytes = kArrBytes * ARRAYS;
+    static constexpr uint32_t kBarOff = kStageBytes * STAGES;
+    static constexpr uint32_t kBytes = kBarOff + 8u * STAGES;
+
+    uint8_t *base;
+
+    __device__ __forceinline__ uint32_t *buf(int s, int array = 0) const
+    {
+        return reinterpret_cast<uint32_t *>(base + s * kStageBytes + array * kArrBytes);
+    }
+    __device__ __forceinline__ uint64_t *bar(int s) const
+    {
+        return reinterpret_cast<uint64_t *>(base + kBarOff) + s;
+    }
+
+    // Thread 0, once: set up the barriers.
+    __device__ __forceinline__ void init() const
+    {
+        for (int s = 0; s < STAGES; ++s) mbar_init(bar(s), 1);
+        fence_barrier_init();
+    }
+
+    // Thread 0: start copying tile `tile` (< the tile count) of each of the
+    // ARRAYS arrays in `srcs` into stage s.
+    __device__ __forceinline__ void issue(int s, const uint32_t *const (&srcs)[ARRAYS], uint32_t tile,
+                                          uint32_t tile_elems, uint32_t n) const
+    {
+        const uint32_t first = tile * tile_elems;
+        const uint32_t bytes = (min(tile_elems, n - first) & ~3u) * 4u;
+        if (bytes != 0u) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar(s), bytes * ARRAYS);
+#pragma unroll
+            for (int a = 0; a < ARRAYS; ++a) bulk_load(buf(s, a), srcs[a] + first, bytes, bar(s));
+        } else {
+            mbar_arrive(bar(s));
+        }
+    }
+
+    // Thread 0: the prologue, the first STAGES tiles of this CTA.
+    __device__ __forceinline__ void prime(const uint32_t *const (&srcs)[ARRAYS], uint32_t tile_elems,
+                                          uint32_t n, uint32_t num_tiles) const
+    {
+        for (int s = 0; s < STAGES; ++s) {
+            const uint32_t t = blockIdx.x + uint32_t(s) * gridDim.x;
+            if (t < num_tiles) issue(s, srcs, t, tile_elems, n);
+        }
+    }
+
+    // Thread 0, after the barrier that ends the use of stage s by tile
+    // `tile`: re-arm s with this CTA's tile STAGES rounds later.
+    __device__ __forceinline__ void refill(int s, const uint32_t *const (&srcs)[ARRAYS], uint32_t tile,
+                                           uint32_t tile_elems, uint32_t n, uint32_t num_tiles) const
+    {
+        const uint32_t t = tile + uint32_t(STAGES) * gridDim.x;
+        if (t < num_tiles) issue(s, srcs, t, tile_elems, n);
+    }
+};
+
+// Elements of tile `tile` that arrive in shared memory (the rest of a ragged
+// last tile is read from global memory).
+__device__ __forceinline__ uint32_t staged_elems(uint32_t tile, uint32_t tile_elems, uint32_t n)
+{
+    const uint32_t first = tile * tile_elems;
+    return min(tile_elems, n - first) & ~3u;
+}
+
+// Vector of 4 elements at tile-local index li: from the stage buffer when it
+// was copied there, otherwise from global memory (elements at or past n read
+// as `fill`).
+__device__ __forceinline__ void stage_load4(const uint32_t *sbuf, const uint32_t *__restrict__ gin,
+                                            uint32_t base, uint32_t li, uint32_t staged, uint32_t n,
+                                            uint32_t fill, uint32_t (&v)[4])
+{
+    if (li + 4u <= staged) {
+        const uint4 q = *reinterpret_cast<const uint4 *>(sbuf + li);
+        v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = (base + li + k < n) ? gin[base + li + k] : fill;
+    }
+}
+
+}  // namespace gcd

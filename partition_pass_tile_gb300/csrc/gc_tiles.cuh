@@ -1,0 +1,487 @@
+// gc_tiles.cuh -- the persistent, pipelined single-pass tile driver shared by
+// every 16-byte-aligned kernel of libgc, and the per-operation tile bodies
+// (exclusive scan, select-if, partition / one-bit split).
+//
+// Every operation of the path has the same two halves ("compaction.cu --
+// Day 33", file header: predicate, scan, scatter): a tile's aggregate (its
+// sum, or how many elements its predicate keeps), and the tile's output once
+// the aggregates of all earlier tiles are known (its exclusive prefix).  The
+// driver runs them as a software pipeline over the tiles a CTA owns:
+//
+//   grid      cooperative (every CTA resident); CTA c of G owns tiles c,
+//             c + G, c + 2G, ...
+//   loads     TMA bulk copies into STAGES shared-memory stage buffers
+//             (gc_pipe.cuh), issued as soon as a stage is free;
+//   iteration k, t = the CTA's k-th tile, p = t - G its previous one:
+//     1. issue the loads of p's window: the aggregates of tiles p - G + 1 ..
+//        p - 1, which their CTAs published a whole iteration earlier;
+//     2. reduce t in shared memory and publish its aggregate at once;
+//     3. finish the window: prefix(p) = run + window, run = prefix(p) +
+//        agg(p), where run is the inclusive prefix of the tile before p
+//        (kept by the CTA, so the walk never goes past it);
+//     4. op.finish: compute and write p's outputs, then re-arm p's stage.
+//   No tile ever waits on another CTA for more than a reduction, and the
+//   window loads are in flight during the reduction.
+//
+// This is the single-pass scan with decoupled look-back of "The CUDA
+// Handbook, ch. 13: Stream compaction" (Listing 13-17 and the scan it builds
+// on) with two changes for a GPU whose HBM wants megabytes in flight: tiles
+// are owned round-robin and prefetched by TMA, and every look-back stops at
+// the CTA's own previous tile, one iteration late, so it is one round of
+// reads of already-published words.
+#pragma once
+
+#include <cstdint>
+
+#include "gc_device.cuh"
+#include "gc_pipe.cuh"
+
+namespace gcd {
+
+// ---------------------------------------------------------------- float-float sums
+// Error-free transformation of a + b (Knuth's TwoSum): s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
+{
+    s = a + b;
+    const float bb = s - a;
+    e = (a - (s - bb)) + (b - bb);
+}
+
+// Window of float32 aggregates summed as an unevaluated float pair per
+// thread and warp, combined in double by thread 0 only (double arithmetic is
+// slow on this GPU, so it stays off the other 255 threads).
+template <int THREADS>
+__device__ __forceinline__ double window_finish_ff(const uint64_t *status, uint32_t lo, uint32_t hi,
+                                                   WindowLoads &wl, uint8_t *ws, uint32_t tile,
+                                                   uint64_t timeout_ns, float *s_hi, float *s_lo)
+{
+    float sh = 0.0f, sl = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kWinPerThread; ++i) {
+        const uint32_t j = lo + threadIdx.x + uint32_t(i) * THREADS;
+        if (j < hi) {
+            uint32_t v = uint32_t(wl.w[i]);
+            if (uint32_t(wl.w[i] >> 32) == kFlagNone) v = await_aggregate(status, j, ws, tile, timeout_ns);
+            float s, e;
+            two_sum(sh, __uint_as_float(v), s, e);
+            sh = s;
+            sl += e;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float oh = __shfl_xor_sync(kFullMask, sh, o);
+        const float ol = __shfl_xor_sync(kFullMask, sl, o);
+        float s, e;
+        two_sum(sh, oh, s, e);
+        sh = s;
+        sl = sl + ol + e;
+    }
+    if ((threadIdx.x & 31) == 0) {
+        s_hi[threadIdx.x >> 5] = sh;
+        s_lo[threadIdx.x >> 5] = sl;
+    }
+    __syncthreads();
+    double t = 0.0;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < THREADS / 32; ++w) t += double(s_hi[w]) + double(s_lo[w]);
+    return t;  // meaningful in thread 0
+}
+
+// ---------------------------------------------------------------- the driver
+template <int THREADS, int STAGES, class Op>
+__device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32_t n,
+                                             uint32_t num_tiles, uint8_t *ws, uint64_t timeout_ns)
+{
+    static_assert(STAGES >= 3, "the tile being reduced, the tile being finished, one in flight");
+    using P = typename Op::template PipeT<STAGES>;
+    constexpr uint32_t TE = Op::kTileElems;
+    constexpr int W = THREADS / 32;
+    __shared__ uint32_t s_red[W];
+    __shared__ uint32_t s_win_u[W];
+    __shared__ double s_win_d[1];
+    __shared__ float s_win_hi[W], s_win_lo[W];
+    __shared__ float s_pref[2];
+    const P pipe{smem};
+    const int tid = threadIdx.x;
+    uint64_t *status = reinterpret_cast<uint64_t *>(ws + kStatusOff);
+
+    if (tid == 0) pipe.init();
+    __syncthreads();
+    if (tid == 0) pipe.prime(op.srcs, TE, n, num_tiles);
+
+    uint32_t run_u = 0u;     // inclusive prefix of the tile before the previous one
+    double run_d = 0.0;      // the same for float32 (thread 0)
+    uint32_t prev_agg = 0u;  // aggregate bits of the previous tile
+    for (uint32_t k = 0;; ++k) {
+        const uint32_t tile = blockIdx.x + k * gridDim.x;
+        const bool have = tile < num_tiles;
+        const bool have_prev = k > 0;
+        const uint32_t prev = tile - gridDim.x;
+
+        WindowLoads wl;
+        if (have_prev) window_issue<THREADS>(status, window_lo(prev), prev, wl);
+
+        uint32_t agg = 0u;
+        if (have) {
+            const int s = int(k % STAGES);
+            mbar_wait(pipe.bar(s), (k / STAGES) & 1u, ws, timeout_ns);
+            const uint32_t base = tile * TE;
+            agg = op.reduce(pipe, s, base, staged_elems(tile, TE, n), n, s_red);
+            if (tid == 0) publish_aggregate(status, tile, agg);
+        }
+
+        if (have_prev) {
+            const int ps = int((k - 1) % STAGES);
+            const uint32_t pbase = prev * TE;
+            const uint32_t pstaged = staged_elems(prev, TE, n);
+            const bool last = prev == num_tiles - 1;
+            if constexpr (Op::kF32) {
+                const double wsum = window_finish_ff<THREADS>(status, window_lo(prev), prev, wl, ws,
+                                                              prev, timeout_ns, s_win_hi, s_win_lo);
+                if (tid == 0) {
+                    const double prefix = run_d + wsum;
+                    run_d = prefix + double(__uint_as_float(prev_agg));
+                    const float ph = float(prefix);
+                    s_pref[0] = ph;
+                    s_pref[1] = float(prefix - double(ph));
+                    s_win_d[0] = run_d;
+                }
+                __syncthreads();
+                op.finish_f32(pipe, ps, pbase, pstaged, n, s_pref[0], s_pref[1], last, s_win_d[0]);
+            } else {
+                uint32_t wsum_u;
+                double unused;
+                window_finish<THREADS, false>(status, window_lo(prev), prev, wl, ws, prev, timeout_ns,
+                                              s_win_u, nullptr, wsum_u, unused);
+                const uint32_t prefix = run_u + wsum_u;
+                run_u = prefix + prev_agg;
+                op.finish(pipe, ps, prev, pbase, pstaged, n, prefix, prev_agg, last);
+            }
+            __syncthreads();  // the previous tile's stage is free again
+            if (tid == 0) pipe.refill(ps, op.srcs, prev, TE, n, num_tiles);
+        }
+        if (!have) break;
+        prev_agg = agg;
+    }
+}
+
+// Grid limit of pipeline_run: the window of a tile must fit kWinPerThread
+// loads per thread.
+template <int THREADS>
+constexpr int pipeline_max_grid() { return kWinPerThread * THREADS + 1; }
+
+// ---------------------------------------------------------------- tile bodies
+
+// Exclusive scan, uint32 (int32 bits) or float32.
+template <int THREADS, int ROWS, bool F32, bool OUT_VEC>
+struct ScanOp {
+    using TT = Tile<THREADS, ROWS>;
+    static constexpr uint32_t kTileElems = TT::kElems;
+    static constexpr bool kF32 = F32;
+    template <int STAGES>
+    using PipeT = Pipe<kTileElems * 4u, STAGES, 1>;
+
+    const uint32_t *srcs[1];
+    uint32_t *out;
+    uint32_t *total;
+
+    template <class P>
+    __device__ __forceinline__ uint32_t reduce(const P &pipe, int s, uint32_t base, uint32_t staged,
+                                               uint32_t n, uint32_t *s_red) const
+    {
+        const int tid = threadIdx.x;
+        if constexpr (F32) {
+            float a = 0.0f;
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                uint32_t x[4];
+                stage_load4(pipe.buf(s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x);
+                a += (__uint_as_float(x[0]) + __uint_as_float(x[1])) +
+                     (__uint_as_float(x[2]) + __uint_as_float(x[3]));
+            }
+            return __float_as_uint(block_sum_all<THREADS>(a, reinterpret_cast<float *>(s_red)));
+        } else {
+            uint32_t a = 0u;
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                uint32_t x[4];
+                stage_load4(pipe.buf(s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x);
+                a += x[0] + x[1] + x[2] + x[3];
+            }
+            return block_sum_all<THREADS>(a, s_red);
+        }
+    }
+
+    template <class P>
+    __device__ __forceinline__ void finish(const P &pipe, int s, uint32_t tile, uint32_t base,
+                                           uint32_t staged, uint32_t n, uint32_t prefix,
+                                           uint32_t agg, bool last) const
+    {
+        __shared__ uint32_t s_chunk[TT::kChunks];
+        const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+        uint32_t x[ROWS][4];
+        uint32_t lane_excl[ROWS];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            stage_load4(pipe.buf(s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x[r]);
+            const uint32_t v = x[r][0] + x[r][1] + x[r][2] + x[r][3];
+            uint32_t incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(kFullMask, incl, o);
+                if (lane >= o) incl += y;
+            }
+            lane_excl[r] = incl - v;
+            if (lane == 31) s_chunk[r * TT::kWarps + warp] = incl;
+        }
+        __syncthreads();
+        if (warp == 0) scan_chunks_warp0<TT>(s_chunk);
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            uint32_t v = prefix + s_chunk[r * TT::kWarps + warp] + lane_excl[r];
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                o[q] = v;
+                v += x[r][q];
+            }
+            store4<OUT_VEC>(out, base + r * TT::kRowElems + 4 * tid, n, o);
+        }
+        if (tid == 0 && total != nullptr && last) *total = prefix + agg;
+        (void)tile;
+    }
+
+    // float32: each output is hi + (lo + local), with hi + lo the tile's
+    // exclusive prefix (a double split into two floats) and local the float
+    // sum inside the tile.
+    template <class P>
+    __device__ __forceinline__ void finish_f32(const P &pipe, int s, uint32_t base, uint32_t staged,
+                                               uint32_t n, float hi, float lo, bool last,
+                                               double inclusive) const
+    {
+        __shared__ float s_chunk[TT::kChunks];
+        const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+        uint32_t x[ROWS][4];
+        float lane_excl[ROWS];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            stage_load4(pipe.buf(s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x[r]);
+            const float v = (__uint_as_float(x[r][0]) + __uint_as_float(x[r][1])) +
+                            (__uint_as_float(x[r][2]) + __uint_as_float(x[r][3]));
+            float incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(kFullMask, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const float ex = __shfl_up_sync(kFullMask, incl, 1);
+            lane_excl[r] = (lane == 0) ? 0.0f : ex;
+            if (lane == 31) s_chunk[r * TT::kWarps + warp] = incl;
+        }
+        __syncthreads();
+        if (warp == 0) scan_chunks_warp0<TT>(s_chunk);
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            float local = s_chunk[r * TT::kWarps + warp] + lane_excl[r];
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                o[q] = __float_as_uint(hi + (lo + local));
+                local += __uint_as_float(x[r][q]);
+            }
+            store4<OUT_VEC>(out, base + r * TT::kRowElems + 4 * tid, n, o);
+        }
+        if (tid == 0 && total != nullptr && last) *total = __float_as_uint(float(inclusive));
+    }
+};
+
+// Predicate masks of one staged tile: bit q of mask[r] says element q of
+// thread's vector r is kept (and lies below n).
+template <class TT, class Pred>
+__device__ __forceinline__ void tile_masks(const uint32_t *sbuf, const uint32_t *gin, uint32_t base,
+                                           uint32_t staged, uint32_t n, const Pred &pred,
+                                           uint32_t (&x)[TT::kRows][4], uint32_t (&mask)[TT::kRows])
+{
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int r = 0; r < TT::kRows; ++r) {
+        const uint32_t li = r * TT::kRowElems + 4 * tid;
+        stage_load4(sbuf, gin, base, li, staged, n, 0u, x[r]);
+        uint32_t m = 0u;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) m |= uint32_t(base + li + q < n && pred(x[r][q])) << q;
+        mask[r] = m;
+    }
+}
+
+template <class TT, class Pred>
+__device__ __forceinline__ uint32_t tile_count(const uint32_t *sbuf, const uint32_t *gin,
+                                               uint32_t base, uint32_t staged, uint32_t n,
+                                               const Pred &pred, uint32_t *s_red)
+{
+    const int tid = threadIdx.x;
+    uint32_t c = 0u;
+#pragma unroll
+    for (int r = 0; r < TT::kRows; ++r) {
+        const uint32_t li = r * TT::kRowElems + 4 * tid;
+        uint32_t x[4];
+        stage_load4(sbuf, gin, base, li, staged, n, 0u, x);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) c += uint32_t(base + li + q < n && pred(x[q]));
+    }
+    return block_sum_all<TT::kThreads>(c, s_red);
+}
+
+// Stable select-if.  The tile's survivors are compacted in place inside its
+// own stage buffer (every element is read into registers before the barrier
+// that precedes the first write, and a survivor's rank never exceeds its
+// index), shifted so that shared and global addresses agree modulo 16 bytes,
+// then written as one contiguous run with 128-bit stores.
+template <int THREADS, int ROWS, class Pred, bool VEC>
+struct SelectOp {
+    using TT = Tile<THREADS, ROWS>;
+    static constexpr uint32_t kTileElems = TT::kElems;
+    static constexpr bool kF32 = false;
+    template <int STAGES>
+    using PipeT = Pipe<kTileElems * 4u, STAGES, 1>;
+
+    const uint32_t *srcs[1];
+    uint32_t *out;
+    uint32_t *count;
+    Pred pred;
+
+    template <class P>
+    __device__ __forceinline__ uint32_t reduce(const P &pipe, int s, uint32_t base, uint32_t staged,
+                                               uint32_t n, uint32_t *s_red) const
+    {
+        return tile_count<TT>(pipe.buf(s), srcs[0], base, staged, n, pred, s_red);
+    }
+
+    template <class P>
+    __device__ __forceinline__ void finish(const P &pipe, int s, uint32_t tile, uint32_t base,
+                                           uint32_t staged, uint32_t n, uint32_t before,
+                                           uint32_t kept, bool last) const
+    {
+        __shared__ uint32_t s_chunk[TT::kChunks];
+        const int warp = threadIdx.x >> 5;
+        uint32_t *buf = pipe.buf(s);
+        uint32_t x[ROWS][4], mask[ROWS], lane_excl[ROWS];
+        tile_masks<TT>(buf, srcs[0], base, staged, n, pred, x, mask);
+        rank_masks<TT>(mask, lane_excl, s_chunk);
+        __syncthreads();
+        if (warp == 0) scan_chunks_warp0<TT>(s_chunk);
+        __syncthreads();
+        const uint32_t shift = VEC ? (before & 3u) : 0u;
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            uint32_t pos = shift + s_chunk[r * TT::kWarps + warp] + lane_excl[r];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if ((mask[r] >> q) & 1u) buf[pos++] = x[r][q];
+        }
+        __syncthreads();
+        store_run<THREADS, VEC>(out, before, buf, shift, kept);
+        if (threadIdx.x == 0 && last) *count = before + kept;
+        (void)tile;
+    }
+};
+
+// Stable partition (and the radix one-bit split, with payloads): kept
+// elements go to [before, before + kept) and rejected ones to
+// T + (base - before) onwards, the i - rank[i] addressing of "compaction.cu
+// -- Day 33" (scatterPartition), with T the total kept from the pre-pass.
+// Both runs are compacted in place in the stage buffer(s) and written with
+// 128-bit stores.
+template <int THREADS, int ROWS, class Pred, bool VEC, bool VALS>
+struct PartitionOp {
+    using TT = Tile<THREADS, ROWS>;
+    static constexpr uint32_t kTileElems = TT::kElems;
+    static constexpr bool kF32 = false;
+    template <int STAGES>
+    using PipeT = Pipe<kTileElems * 4u, STAGES, VALS ? 2 : 1>;
+
+    const uint32_t *srcs[VALS ? 2 : 1];
+    uint32_t *keys_out;
+    uint32_t *vals_out;
+    const uint32_t *true_total;  // written by the pre-pass kernel
+    uint8_t *ws;
+    Pred pred;
+
+    template <class P>
+    __device__ __forceinline__ uint32_t reduce(const P &pipe, int s, uint32_t base, uint32_t staged,
+                                               uint32_t n, uint32_t *s_red) const
+    {
+        return tile_count<TT>(pipe.buf(s), srcs[0], base, staged, n, pred, s_red);
+    }
+
+    template <class P>
+    __device__ __forceinline__ void finish(const P &pipe, int s, uint32_t tile, uint32_t base,
+                                           uint32_t staged, uint32_t n, uint32_t before,
+                                           uint32_t kept, bool last) const
+    {
+        __shared__ uint32_t s_chunk[TT::kChunks];
+        const int tid = threadIdx.x, warp = tid >> 5;
+        uint32_t *kbuf = pipe.buf(s, 0);
+        uint32_t *vbuf = pipe.buf(s, VALS ? 1 : 0);
+        uint32_t x[ROWS][4], mask[ROWS], lane_excl[ROWS];
+        uint32_t v[VALS ? ROWS : 1][4];
+        tile_masks<TT>(kbuf, srcs[0], base, staged, n, pred, x, mask);
+        if (VALS) {
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+                stage_load4(vbuf, srcs[VALS ? 1 : 0], base, r * TT::kRowElems + 4 * tid, staged, n,
+                            0u, v[VALS ? r : 0]);
+        }
+        rank_masks<TT>(mask, lane_excl, s_chunk);
+        const uint32_t T = *true_total;
+        __syncthreads();
+        if (warp == 0) scan_chunks_warp0<TT>(s_chunk);
+        __syncthreads();
+
+        const uint32_t valid = min(kTileElems, n - base);
+        uint32_t rejected = valid - kept;
+        const uint32_t dst_kept = before;
+        const uint32_t dst_rej = T + (base - before);
+        uint32_t kept_len = kept;
+        // Both runs must lie inside [0, n), which holds when T is the true
+        // count; a wrong T (a workspace corrupted between the two kernels) is
+        // recorded and the stores are skipped.
+        if (uint64_t(dst_rej) + rejected > n || uint64_t(dst_kept) + kept > T) {
+            if (tid == 0) record_error(ws, kDeviceCheckCode, tile);
+            kept_len = 0u;
+            rejected = 0u;
+        }
+        const uint32_t sh_kept = VEC ? (dst_kept & 3u) : 0u;
+        const uint32_t rej_region = (sh_kept + kept + 3u) & ~3u;
+        const uint32_t sh_rej = rej_region + (VEC ? (dst_rej & 3u) : 0u);
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            const uint32_t local0 = r * TT::kRowElems + 4 * tid;
+            uint32_t ranked = s_chunk[r * TT::kWarps + warp] + lane_excl[r];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t local = local0 + q;
+                if (base + local < n) {
+                    const bool keep = (mask[r] >> q) & 1u;
+                    const uint32_t slot = keep ? sh_kept + ranked : sh_rej + (local - ranked);
+                    kbuf[slot] = x[r][q];
+                    if (VALS) vbuf[slot] = v[VALS ? r : 0][q];
+                    ranked += keep ? 1u : 0u;
+                }
+            }
+        }
+        __syncthreads();
+        store_run<THREADS, VEC>(keys_out, dst_kept, kbuf, sh_kept, kept_len);
+        store_run<THREADS, VEC>(keys_out, dst_rej, kbuf, sh_rej, rejected);
+        if (VALS) {
+            store_run<THREADS, VEC>(vals_out, dst_kept, vbuf, sh_kept, kept_len);
+            store_run<THREADS, VEC>(vals_out, dst_rej, vbuf, sh_rej, rejected);
+        }
+        (void)last;
+    }
+};
+
+}  // namespace gcd

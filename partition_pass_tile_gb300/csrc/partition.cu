@@ -18,6 +18,7 @@
 // over the input gives T for all 32 splits.
 #include "gc_device.cuh"
 #include "gc_internal.h"
+#include "gc_launch.cuh"
 
 namespace {
 
@@ -25,7 +26,7 @@ using namespace gcd;
 
 constexpr int kPad = 12;  // shared staging slack: two runs, each shifted by up to 3
 
-template <class Pred, int THREADS, int ROWS, bool VEC, bool VALS>
+template <class Pred, int THREADS, int ROWS, bool VEC, bool VALS, bool LB>
 __global__ void __launch_bounds__(THREADS)
 partition_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__restrict__ vals_in,
                  uint32_t *__restrict__ keys_out, uint32_t *__restrict__ vals_out, uint32_t n,
@@ -35,7 +36,8 @@ partition_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__restric
     using TT = Tile<THREADS, ROWS>;
     __shared__ uint32_t s_tile;
     __shared__ uint32_t s_chunk[TT::kChunks];
-    __shared__ uint32_t s_before, s_kept, s_total;
+    __shared__ PrefixSmem s_ps;
+    __shared__ uint32_t s_total;
     __shared__ __align__(16) uint32_t s_keys[TT::kElems + kPad];
     __shared__ __align__(16) uint32_t s_vals[VALS ? TT::kElems + kPad : 4];
 
@@ -62,19 +64,9 @@ partition_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__restric
     rank_masks<TT>(mask, lane_excl, s_chunk);
     __syncthreads();
 
-    if (warp == 0) {
-        const uint32_t kept = scan_chunks_warp0<TT>(s_chunk);
-        uint64_t *status = reinterpret_cast<uint64_t *>(ws + kStatusOff);
-        const uint32_t before = lookback_u32(status, tile, kept, ws, timeout_ns);
-        if (lane == 0) {
-            s_before = before;
-            s_kept = kept;
-            s_total = *true_total;
-        }
-    }
-    __syncthreads();
-
-    const uint32_t before = s_before, kept = s_kept;
+    if (tid == 0) s_total = *true_total;
+    uint32_t before, kept;
+    resolve_prefix_u32<TT, LB>(s_chunk, tile, ws, timeout_ns, s_ps, before, kept);
     const uint32_t valid = min(uint32_t(TT::kElems), n - base);
     const uint32_t rejected = valid - kept;
     const uint32_t dst_kept = before;                      // rank of the tile's first kept element
@@ -264,11 +256,47 @@ int reduce_grid(uint32_t n, int threads)
     return int(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
+template <int PT, int PR, int PS, class Pred, bool VALS>
+cudaError_t run_partition_pipe(const uint32_t *kin, const uint32_t *vin, uint32_t *kout,
+                               uint32_t *vout, uint32_t n, const uint32_t *true_total, Pred pred,
+                               uint8_t *ws, cudaStream_t s, const gch::LaunchOpts &o)
+{
+    const bool vec = gch::aligned16(kout) && (!VALS || gch::aligned16(vout));
+    auto fill = [&](auto &op) {
+        op.srcs[0] = kin;
+        if constexpr (VALS) op.srcs[VALS ? 1 : 0] = vin;
+        op.keys_out = kout;
+        op.vals_out = vout;
+        op.true_total = true_total;
+        op.ws = ws;
+        op.pred = pred;
+    };
+    if (vec) {
+        gcd::PartitionOp<PT, PR, Pred, true, VALS> op{};
+        fill(op);
+        return gcd::launch_pipeline<PT, PS>(op, n, ws, s, o.timeout_ns);
+    }
+    gcd::PartitionOp<PT, PR, Pred, false, VALS> op{};
+    fill(op);
+    return gcd::launch_pipeline<PT, PS>(op, n, ws, s, o.timeout_ns);
+}
+
 template <class Pred, bool VALS>
 cudaError_t run_partition_pass(const uint32_t *kin, const uint32_t *vin, uint32_t *kout,
                                uint32_t *vout, uint32_t n, const uint32_t *true_total, Pred pred,
                                uint8_t *ws, cudaStream_t s, const gch::LaunchOpts &o, bool split)
 {
+    if (gch::aligned16(kin) && (!VALS || gch::aligned16(vin)) && !o.skip_first_tile) {
+        cudaError_t e;
+        if (split)
+            e = run_partition_pipe<gch::kSplitPipeThreads, gch::kSplitPipeRows, gch::kSplitPipeStages,
+                                   Pred, VALS>(kin, vin, kout, vout, n, true_total, pred, ws, s, o);
+        else
+            e = run_partition_pipe<gch::kPartPipeThreads, gch::kPartPipeRows, gch::kPartPipeStages,
+                                   Pred, VALS>(kin, vin, kout, vout, n, true_total, pred, ws, s, o);
+        if (e == cudaSuccess) return e;
+        (void)cudaGetLastError();  // cooperative grid refused: one tile per CTA instead
+    }
     constexpr int PT = gch::kPartThreads, PR = gch::kPartRows;
     constexpr int ST = gch::kSplitThreads, SR = gch::kSplitRows;
     const uint32_t tile = split ? gch::tile_elems(ST, SR) : gch::tile_elems(PT, PR);
@@ -281,17 +309,17 @@ cudaError_t run_partition_pass(const uint32_t *kin, const uint32_t *vin, uint32_
                      (!VALS || (gch::aligned16(vin) && gch::aligned16(vout)));
     if (split) {
         if (vec)
-            partition_kernel<Pred, ST, SR, true, VALS><<<grid, ST, 0, s>>>(
+            partition_kernel<Pred, ST, SR, true, VALS, gch::kCtaLookback><<<grid, ST, 0, s>>>(
                 kin, vin, kout, vout, n, tiles, true_total, pred, ws, o.timeout_ns);
         else
-            partition_kernel<Pred, ST, SR, false, VALS><<<grid, ST, 0, s>>>(
+            partition_kernel<Pred, ST, SR, false, VALS, gch::kCtaLookback><<<grid, ST, 0, s>>>(
                 kin, vin, kout, vout, n, tiles, true_total, pred, ws, o.timeout_ns);
     } else {
         if (vec)
-            partition_kernel<Pred, PT, PR, true, VALS><<<grid, PT, 0, s>>>(
+            partition_kernel<Pred, PT, PR, true, VALS, gch::kCtaLookback><<<grid, PT, 0, s>>>(
                 kin, vin, kout, vout, n, tiles, true_total, pred, ws, o.timeout_ns);
         else
-            partition_kernel<Pred, PT, PR, false, VALS><<<grid, PT, 0, s>>>(
+            partition_kernel<Pred, PT, PR, false, VALS, gch::kCtaLookback><<<grid, PT, 0, s>>>(
                 kin, vin, kout, vout, n, tiles, true_total, pred, ws, o.timeout_ns);
     }
     return cudaGetLastError();
@@ -320,8 +348,8 @@ cudaError_t dispatch_partition(const uint32_t *in, uint32_t *out, uint32_t *coun
 
 namespace gch {
 
-uint32_t partition_tile_elems() { return tile_elems(kPartThreads, kPartRows); }
-uint32_t split_tile_elems() { return tile_elems(kSplitThreads, kSplitRows); }
+uint32_t partition_tile_elems() { return tile_elems(kPartPipeThreads, kPartPipeRows); }
+uint32_t split_tile_elems() { return tile_elems(kSplitPipeThreads, kSplitPipeRows); }
 
 cudaError_t launch_partition(const void *in, void *out, uint32_t *count_true, uint32_t n,
                              gc_dtype dt, gc_pred p, uint8_t *ws, cudaStream_t s,

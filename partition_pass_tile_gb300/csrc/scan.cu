@@ -22,12 +22,13 @@
 // thread's elements.
 #include "gc_device.cuh"
 #include "gc_internal.h"
+#include "gc_launch.cuh"
 
 namespace {
 
 using namespace gcd;
 
-template <int THREADS, int ROWS, bool VEC>
+template <int THREADS, int ROWS, bool VEC, bool LB>
 __global__ void __launch_bounds__(THREADS)
 scan_u32_kernel(const uint32_t *in, uint32_t *out, uint32_t *total, uint32_t n,
                 uint32_t num_tiles, uint8_t *ws, uint64_t timeout_ns)
@@ -35,7 +36,7 @@ scan_u32_kernel(const uint32_t *in, uint32_t *out, uint32_t *total, uint32_t n,
     using TT = Tile<THREADS, ROWS>;
     __shared__ uint32_t s_tile;
     __shared__ uint32_t s_chunk[TT::kChunks];
-    __shared__ uint32_t s_prefix;
+    __shared__ PrefixSmem s_ps;
 
     const uint32_t tile = claim_tile(ws, &s_tile);
     if (tile >= num_tiles) return;  // only with the skip-first-tile test hook
@@ -62,18 +63,9 @@ scan_u32_kernel(const uint32_t *in, uint32_t *out, uint32_t *total, uint32_t n,
     }
     __syncthreads();
 
-    if (warp == 0) {
-        const uint32_t agg = scan_chunks_warp0<TT>(s_chunk);
-        uint64_t *status = reinterpret_cast<uint64_t *>(ws + kStatusOff);
-        const uint32_t excl = lookback_u32(status, tile, agg, ws, timeout_ns);
-        if (lane == 0) {
-            s_prefix = excl;
-            if (total != nullptr && tile == num_tiles - 1) *total = excl + agg;
-        }
-    }
-    __syncthreads();
-
-    const uint32_t prefix = s_prefix;
+    uint32_t prefix, agg;
+    resolve_prefix_u32<TT, LB>(s_chunk, tile, ws, timeout_ns, s_ps, prefix, agg);
+    if (tid == 0 && total != nullptr && tile == num_tiles - 1) *total = prefix + agg;
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
         uint32_t v = prefix + s_chunk[r * TT::kWarps + warp] + lane_excl[r];
@@ -92,7 +84,7 @@ scan_u32_kernel(const uint32_t *in, uint32_t *out, uint32_t *total, uint32_t n,
 // hi + lo (hi = the double rounded to float, lo = the remainder rounded to
 // float), and each output is hi + (lo + local).  The carry between tiles
 // therefore never rounds to float32 before the last add of each element.
-template <int THREADS, int ROWS, bool VEC>
+template <int THREADS, int ROWS, bool VEC, bool LB>
 __global__ void __launch_bounds__(THREADS)
 scan_f32_kernel(const uint32_t *in_bits, uint32_t *out_bits, uint32_t *total_bits, uint32_t n,
                 uint32_t num_tiles, uint8_t *ws, double *prefix64, uint64_t timeout_ns)
@@ -100,7 +92,7 @@ scan_f32_kernel(const uint32_t *in_bits, uint32_t *out_bits, uint32_t *total_bit
     using TT = Tile<THREADS, ROWS>;
     __shared__ uint32_t s_tile;
     __shared__ float s_chunk[TT::kChunks];
-    __shared__ float s_hi, s_lo;
+    __shared__ PrefixSmem s_ps;
 
     const uint32_t tile = claim_tile(ws, &s_tile);
     if (tile >= num_tiles) return;
@@ -129,21 +121,13 @@ scan_f32_kernel(const uint32_t *in_bits, uint32_t *out_bits, uint32_t *total_bit
     }
     __syncthreads();
 
-    if (warp == 0) {
-        const float agg = scan_chunks_warp0<TT>(s_chunk);
-        uint64_t *status = reinterpret_cast<uint64_t *>(ws + kStatusOff);
-        const double excl = lookback_f32(status, prefix64, tile, agg, ws, timeout_ns);
-        if (lane == 0) {
-            const float hi = float(excl);
-            s_hi = hi;
-            s_lo = float(excl - double(hi));
-            if (total_bits != nullptr && tile == num_tiles - 1)
-                *total_bits = __float_as_uint(float(excl + double(agg)));
-        }
-    }
-    __syncthreads();
-
-    const float hi = s_hi, lo = s_lo;
+    double excl;
+    float agg;
+    resolve_prefix_f32<TT, LB>(s_chunk, tile, ws, prefix64, timeout_ns, s_ps, excl, agg);
+    if (tid == 0 && total_bits != nullptr && tile == num_tiles - 1)
+        *total_bits = __float_as_uint(float(excl + double(agg)));
+    const float hi = float(excl);
+    const float lo = float(excl - double(hi));
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
         float local = s_chunk[r * TT::kWarps + warp] + lane_excl[r];
@@ -161,35 +145,65 @@ scan_f32_kernel(const uint32_t *in_bits, uint32_t *out_bits, uint32_t *total_bit
 
 namespace gch {
 
-uint32_t scan_tile_elems() { return tile_elems(kScanThreads, kScanRows); }
+uint32_t scan_tile_elems() { return tile_elems(kScanPipeThreads, kScanPipeRows); }
+
+namespace {
+
+template <bool F32, bool OUT_VEC>
+cudaError_t launch_scan_pipe(const uint32_t *in, uint32_t *out, uint32_t *total, uint32_t n,
+                             uint8_t *ws, cudaStream_t s, const LaunchOpts &o)
+{
+    using Op = gcd::ScanOp<kScanPipeThreads, kScanPipeRows, F32, OUT_VEC>;
+    Op op{{in}, out, total};
+    return gcd::launch_pipeline<kScanPipeThreads, kScanPipeStages>(op, n, ws, s, o.timeout_ns);
+}
+
+}  // namespace
 
 cudaError_t launch_scan(const void *in, void *out, void *total, uint32_t n, gc_dtype dt,
                         uint8_t *ws, cudaStream_t s, const LaunchOpts &o)
 {
-    const uint32_t tile = scan_tile_elems();
+    auto *i = static_cast<const uint32_t *>(in);
+    auto *u = static_cast<uint32_t *>(out);
+    auto *t = static_cast<uint32_t *>(total);
+    cudaError_t e;
+    if (aligned16(in) && !o.skip_first_tile) {
+        const bool ov = aligned16(out);
+        if (dt == GC_F32)
+            e = ov ? launch_scan_pipe<true, true>(i, u, t, n, ws, s, o)
+                   : launch_scan_pipe<true, false>(i, u, t, n, ws, s, o);
+        else
+            e = ov ? launch_scan_pipe<false, true>(i, u, t, n, ws, s, o)
+                   : launch_scan_pipe<false, false>(i, u, t, n, ws, s, o);
+        if (e == cudaSuccess) return e;
+        // The device cannot hold the whole cooperative grid right now (another
+        // context holds SMs): fall through to the kernel that needs no
+        // co-residency.  Clear the launch error first.
+        (void)cudaGetLastError();
+    }
+    // Unaligned input (or the test hook): one tile per CTA, loads straight
+    // into registers.
+    const uint32_t tile = tile_elems(kScanThreads, kScanRows);
     const uint32_t tiles = uint32_t(ceil_div(n, tile));
-    cudaError_t e = reset_tiles(ws, tiles, s, o.skip_first_tile);
+    e = reset_tiles(ws, tiles, s, o.skip_first_tile);
     if (e != cudaSuccess) return e;
     const bool vec = aligned16(in) && aligned16(out);
     const uint32_t grid = o.skip_first_tile ? tiles - 1 : tiles;
     if (grid == 0) return cudaSuccess;
-    auto *i = static_cast<const uint32_t *>(in);
-    auto *u = static_cast<uint32_t *>(out);
-    auto *t = static_cast<uint32_t *>(total);
     if (dt == GC_F32) {
         double *prefix64 = reinterpret_cast<double *>(ws + kHeaderBytes + status_bytes(tiles));
         if (vec)
-            scan_f32_kernel<kScanThreads, kScanRows, true>
+            scan_f32_kernel<kScanThreads, kScanRows, true, kCtaLookback>
                 <<<grid, kScanThreads, 0, s>>>(i, u, t, n, tiles, ws, prefix64, o.timeout_ns);
         else
-            scan_f32_kernel<kScanThreads, kScanRows, false>
+            scan_f32_kernel<kScanThreads, kScanRows, false, kCtaLookback>
                 <<<grid, kScanThreads, 0, s>>>(i, u, t, n, tiles, ws, prefix64, o.timeout_ns);
     } else {
         if (vec)
-            scan_u32_kernel<kScanThreads, kScanRows, true>
+            scan_u32_kernel<kScanThreads, kScanRows, true, kCtaLookback>
                 <<<grid, kScanThreads, 0, s>>>(i, u, t, n, tiles, ws, o.timeout_ns);
         else
-            scan_u32_kernel<kScanThreads, kScanRows, false>
+            scan_u32_kernel<kScanThreads, kScanRows, false, kCtaLookback>
                 <<<grid, kScanThreads, 0, s>>>(i, u, t, n, tiles, ws, o.timeout_ns);
     }
     return cudaGetLastError();

@@ -22,13 +22,14 @@
 // The input is read once; only survivors and the count are written.
 #include "gc_device.cuh"
 #include "gc_internal.h"
+#include "gc_launch.cuh"
 
 
 namespace {
 
 using namespace gcd;
 
-template <class Pred, int THREADS, int ROWS, bool VEC>
+template <class Pred, int THREADS, int ROWS, bool VEC, bool LB>
 __global__ void __launch_bounds__(THREADS)
 select_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, uint32_t *count,
               uint32_t n, uint32_t num_tiles, Pred pred, uint8_t *ws, uint64_t timeout_ns)
@@ -36,7 +37,7 @@ select_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, uint3
     using TT = Tile<THREADS, ROWS>;
     __shared__ uint32_t s_tile;
     __shared__ uint32_t s_chunk[TT::kChunks];
-    __shared__ uint32_t s_base, s_kept;
+    __shared__ PrefixSmem s_ps;
     __shared__ __align__(16) uint32_t s_buf[TT::kElems + 4];
 
     const uint32_t tile = claim_tile(ws, &s_tile);
@@ -60,19 +61,9 @@ select_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, uint3
     rank_masks<TT>(mask, lane_excl, s_chunk);
     __syncthreads();
 
-    if (warp == 0) {
-        const uint32_t kept = scan_chunks_warp0<TT>(s_chunk);
-        uint64_t *status = reinterpret_cast<uint64_t *>(ws + kStatusOff);
-        const uint32_t before = lookback_u32(status, tile, kept, ws, timeout_ns);
-        if (lane == 0) {
-            s_base = before;
-            s_kept = kept;
-            if (tile == num_tiles - 1) *count = before + kept;
-        }
-    }
-    __syncthreads();
-
-    const uint32_t out_base = s_base;
+    uint32_t out_base, kept;
+    resolve_prefix_u32<TT, LB>(s_chunk, tile, ws, timeout_ns, s_ps, out_base, kept);
+    if (tid == 0 && tile == num_tiles - 1) *count = out_base + kept;
     const uint32_t shift = VEC ? (out_base & 3u) : 0u;
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
@@ -83,7 +74,7 @@ select_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, uint3
         }
     }
     __syncthreads();
-    store_run<THREADS, VEC>(out, out_base, s_buf, shift, s_kept);
+    store_run<THREADS, VEC>(out, out_base, s_buf, shift, kept);
 }
 
 // Comparison path ("compaction.cu -- Day 33", compactAtomic): one counter
@@ -128,6 +119,20 @@ template <class Pred>
 cudaError_t dispatch_select(const uint32_t *in, uint32_t *out, uint32_t *count, uint32_t n,
                             Pred pred, uint8_t *ws, cudaStream_t s, const gch::LaunchOpts &o)
 {
+    if (gch::aligned16(in) && !o.skip_first_tile) {
+        constexpr int PT = gch::kSelectPipeThreads, PR = gch::kSelectPipeRows;
+        constexpr int PS = gch::kSelectPipeStages;
+        cudaError_t e;
+        if (gch::aligned16(out)) {
+            gcd::SelectOp<PT, PR, Pred, true> op{{in}, out, count, pred};
+            e = gcd::launch_pipeline<PT, PS>(op, n, ws, s, o.timeout_ns);
+        } else {
+            gcd::SelectOp<PT, PR, Pred, false> op{{in}, out, count, pred};
+            e = gcd::launch_pipeline<PT, PS>(op, n, ws, s, o.timeout_ns);
+        }
+        if (e == cudaSuccess) return e;
+        (void)cudaGetLastError();  // cooperative grid refused: one tile per CTA instead
+    }
     constexpr int T = gch::kSelectThreads, R = gch::kSelectRows;
     const uint32_t tiles = uint32_t(gch::ceil_div(n, gch::tile_elems(T, R)));
     cudaError_t e = gch::reset_tiles(ws, tiles, s, o.skip_first_tile);
@@ -135,9 +140,9 @@ cudaError_t dispatch_select(const uint32_t *in, uint32_t *out, uint32_t *count, 
     const uint32_t grid = o.skip_first_tile ? tiles - 1 : tiles;
     if (grid == 0) return cudaSuccess;
     if (gch::aligned16(in) && gch::aligned16(out))
-        select_kernel<Pred, T, R, true><<<grid, T, 0, s>>>(in, out, count, n, tiles, pred, ws, o.timeout_ns);
+        select_kernel<Pred, T, R, true, gch::kCtaLookback><<<grid, T, 0, s>>>(in, out, count, n, tiles, pred, ws, o.timeout_ns);
     else
-        select_kernel<Pred, T, R, false><<<grid, T, 0, s>>>(in, out, count, n, tiles, pred, ws, o.timeout_ns);
+        select_kernel<Pred, T, R, false, gch::kCtaLookback><<<grid, T, 0, s>>>(in, out, count, n, tiles, pred, ws, o.timeout_ns);
     return cudaGetLastError();
 }
 
@@ -160,7 +165,7 @@ cudaError_t dispatch_atomic(const uint32_t *in, uint32_t *out, uint32_t *count, 
 
 namespace gch {
 
-uint32_t select_tile_elems() { return tile_elems(kSelectThreads, kSelectRows); }
+uint32_t select_tile_elems() { return tile_elems(kSelectPipeThreads, kSelectPipeRows); }
 uint32_t atomic_tile_elems() { return tile_elems(kAtomicThreads, kAtomicRows); }
 
 cudaError_t launch_select(const void *in, void *out, uint32_t *count, uint32_t n, gc_dtype dt,
