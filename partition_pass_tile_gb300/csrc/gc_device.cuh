@@ -309,11 +309,12 @@ __device__ __forceinline__ void load4(const uint32_t *__restrict__ in, uint32_t 
     }
 }
 
+// full_vec: the caller knows the vector is whole and 16-byte aligned.
 template <bool VEC>
 __device__ __forceinline__ void store4(uint32_t *__restrict__ out, uint32_t idx, uint32_t n,
-                                       const uint32_t (&v)[4])
+                                       const uint32_t (&v)[4], bool full_vec = false)
 {
-    if (VEC && idx + 4u <= n) {
+    if (full_vec || (VEC && idx + 4u <= n)) {
         __stcs(reinterpret_cast<uint4 *>(out + idx), make_uint4(v[0], v[1], v[2], v[3]));
     } else {
 #pragma unroll

@@ -184,12 +184,14 @@ __device__ __forceinline__ uint32_t staged_elems(uint32_t tile, uint32_t tile_el
 
 // Vector of 4 elements at tile-local index li: from the stage buffer when it
 // was copied there, otherwise from global memory (elements at or past n read
-// as `fill`).
+// as `fill`).  FULL: the whole tile is staged (every tile but a ragged last
+// one), so no test is needed.
+template <bool FULL = false>
 __device__ __forceinline__ void stage_load4(const uint32_t *sbuf, const uint32_t *__restrict__ gin,
                                             uint32_t base, uint32_t li, uint32_t staged, uint32_t n,
                                             uint32_t fill, uint32_t (&v)[4])
 {
-    if (li + 4u <= staged) {
+    if (FULL || li + 4u <= staged) {
         const uint4 q = *reinterpret_cast<const uint4 *>(sbuf + li);
         v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
     } else {

@@ -47,13 +47,31 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
     e = (a - (s - bb)) + (b - bb);
 }
 
-// Window of float32 aggregates summed as an unevaluated float pair per
-// thread and warp, combined in double by thread 0 only (double arithmetic is
-// slow on this GPU, so it stays off the other 255 threads).
+// Knuth's FastTwoSum, for |a| >= |b|: renormalises a float pair.
+__device__ __forceinline__ void fast_two_sum(float a, float b, float &s, float &e)
+{
+    s = a + b;
+    e = b - (s - a);
+}
+
+// (ah + al) + (bh + bl) as a normalised float pair (double-float addition).
+__device__ __forceinline__ void ff_add(float ah, float al, float bh, float bl, float &sh, float &sl)
+{
+    float s, e;
+    two_sum(ah, bh, s, e);
+    e += al + bl;
+    fast_two_sum(s, e, sh, sl);
+}
+
+// Window of float32 aggregates summed as an unevaluated float pair
+// (double-float arithmetic, about 48 significant bits), per thread, across
+// the warp and across the CTA; every thread gets the pair.  No double
+// arithmetic: it is slow on this GPU.
 template <int THREADS>
-__device__ __forceinline__ double window_finish_ff(const uint64_t *status, uint32_t lo, uint32_t hi,
-                                                   WindowLoads &wl, uint8_t *ws, uint32_t tile,
-                                                   uint64_t timeout_ns, float *s_hi, float *s_lo)
+__device__ __forceinline__ void window_finish_ff(const uint64_t *status, uint32_t lo, uint32_t hi,
+                                                 WindowLoads &wl, uint8_t *ws, uint32_t tile,
+                                                 uint64_t timeout_ns, float *s_hi, float *s_lo,
+                                                 float &out_hi, float &out_lo)
 {
     float sh = 0.0f, sl = 0.0f;
 #pragma unroll
@@ -62,30 +80,25 @@ __device__ __forceinline__ double window_finish_ff(const uint64_t *status, uint3
         if (j < hi) {
             uint32_t v = uint32_t(wl.w[i]);
             if (uint32_t(wl.w[i] >> 32) == kFlagNone) v = await_aggregate(status, j, ws, tile, timeout_ns);
-            float s, e;
-            two_sum(sh, __uint_as_float(v), s, e);
-            sh = s;
-            sl += e;
+            ff_add(sh, sl, __uint_as_float(v), 0.0f, sh, sl);
         }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float oh = __shfl_xor_sync(kFullMask, sh, o);
         const float ol = __shfl_xor_sync(kFullMask, sl, o);
-        float s, e;
-        two_sum(sh, oh, s, e);
-        sh = s;
-        sl = sl + ol + e;
+        ff_add(sh, sl, oh, ol, sh, sl);
     }
     if ((threadIdx.x & 31) == 0) {
         s_hi[threadIdx.x >> 5] = sh;
         s_lo[threadIdx.x >> 5] = sl;
     }
     __syncthreads();
-    double t = 0.0;
-    if (threadIdx.x == 0)
-        for (int w = 0; w < THREADS / 32; ++w) t += double(s_hi[w]) + double(s_lo[w]);
-    return t;  // meaningful in thread 0
+    float th = 0.0f, tl = 0.0f;
+#pragma unroll
+    for (int w = 0; w < THREADS / 32; ++w) ff_add(th, tl, s_hi[w], s_lo[w], th, tl);
+    out_hi = th;
+    out_lo = tl;
 }
 
 // ---------------------------------------------------------------- the driver
@@ -99,9 +112,7 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
     constexpr int W = THREADS / 32;
     __shared__ uint32_t s_red[W];
     __shared__ uint32_t s_win_u[W];
-    __shared__ double s_win_d[1];
     __shared__ float s_win_hi[W], s_win_lo[W];
-    __shared__ float s_pref[2];
     const P pipe{smem};
     const int tid = threadIdx.x;
     uint64_t *status = reinterpret_cast<uint64_t *>(ws + kStatusOff);
@@ -111,8 +122,9 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
     if (tid == 0) pipe.prime(op.srcs, TE, n, num_tiles);
 
     uint32_t run_u = 0u;     // inclusive prefix of the tile before the previous one
-    double run_d = 0.0;      // the same for float32 (thread 0)
+    float run_h = 0.0f, run_l = 0.0f;  // the same for float32, as a float pair
     uint32_t prev_agg = 0u;  // aggregate bits of the previous tile
+    typename Op::Carry cur{}, prv{};  // per-thread results of a reduction kept for its finish
     for (uint32_t k = 0;; ++k) {
         const uint32_t tile = blockIdx.x + k * gridDim.x;
         const bool have = tile < num_tiles;
@@ -127,7 +139,11 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
             const int s = int(k % STAGES);
             mbar_wait(pipe.bar(s), (k / STAGES) & 1u, ws, timeout_ns);
             const uint32_t base = tile * TE;
-            agg = op.reduce(pipe, s, base, staged_elems(tile, TE, n), n, s_red);
+            const uint32_t staged = staged_elems(tile, TE, n);
+            if (staged == TE)
+                agg = op.template reduce<true>(pipe, s, base, staged, n, s_red, cur);
+            else
+                agg = op.template reduce<false>(pipe, s, base, staged, n, s_red, cur);
             if (tid == 0) publish_aggregate(status, tile, agg);
         }
 
@@ -137,18 +153,16 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
             const uint32_t pstaged = staged_elems(prev, TE, n);
             const bool last = prev == num_tiles - 1;
             if constexpr (Op::kF32) {
-                const double wsum = window_finish_ff<THREADS>(status, window_lo(prev), prev, wl, ws,
-                                                              prev, timeout_ns, s_win_hi, s_win_lo);
-                if (tid == 0) {
-                    const double prefix = run_d + wsum;
-                    run_d = prefix + double(__uint_as_float(prev_agg));
-                    const float ph = float(prefix);
-                    s_pref[0] = ph;
-                    s_pref[1] = float(prefix - double(ph));
-                    s_win_d[0] = run_d;
-                }
-                __syncthreads();
-                op.finish_f32(pipe, ps, pbase, pstaged, n, s_pref[0], s_pref[1], last, s_win_d[0]);
+                float wh, wl_;
+                window_finish_ff<THREADS>(status, window_lo(prev), prev, wl, ws, prev, timeout_ns,
+                                          s_win_hi, s_win_lo, wh, wl_);
+                float ph, pl;
+                ff_add(run_h, run_l, wh, wl_, ph, pl);  // prefix(p) = run + window
+                ff_add(ph, pl, __uint_as_float(prev_agg), 0.0f, run_h, run_l);
+                if (pstaged == TE)
+                    op.template finish_f32<true>(pipe, ps, pbase, pstaged, n, ph, pl, last, run_h + run_l, prv);
+                else
+                    op.template finish_f32<false>(pipe, ps, pbase, pstaged, n, ph, pl, last, run_h + run_l, prv);
             } else {
                 uint32_t wsum_u;
                 double unused;
@@ -156,13 +170,17 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
                                               s_win_u, nullptr, wsum_u, unused);
                 const uint32_t prefix = run_u + wsum_u;
                 run_u = prefix + prev_agg;
-                op.finish(pipe, ps, prev, pbase, pstaged, n, prefix, prev_agg, last);
+                if (pstaged == TE)
+                    op.template finish<true>(pipe, ps, prev, pbase, pstaged, n, prefix, prev_agg, last, prv);
+                else
+                    op.template finish<false>(pipe, ps, prev, pbase, pstaged, n, prefix, prev_agg, last, prv);
             }
             __syncthreads();  // the previous tile's stage is free again
             if (tid == 0) pipe.refill(ps, op.srcs, prev, TE, n, num_tiles);
         }
         if (!have) break;
         prev_agg = agg;
+        prv = cur;
     }
 }
 
@@ -186,9 +204,11 @@ struct ScanOp {
     uint32_t *out;
     uint32_t *total;
 
-    template <class P>
+    struct Carry {};
+
+    template <bool FULL, class P>
     __device__ __forceinline__ uint32_t reduce(const P &pipe, int s, uint32_t base, uint32_t staged,
-                                               uint32_t n, uint32_t *s_red) const
+                                               uint32_t n, uint32_t *s_red, Carry &) const
     {
         const int tid = threadIdx.x;
         if constexpr (F32) {
@@ -196,7 +216,7 @@ struct ScanOp {
 #pragma unroll
             for (int r = 0; r < ROWS; ++r) {
                 uint32_t x[4];
-                stage_load4(pipe.buf(s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x);
+                stage_load4<FULL>(pipe.buf(s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x);
                 a += (__uint_as_float(x[0]) + __uint_as_float(x[1])) +
                      (__uint_as_float(x[2]) + __uint_as_float(x[3]));
             }
@@ -206,17 +226,17 @@ struct ScanOp {
 #pragma unroll
             for (int r = 0; r < ROWS; ++r) {
                 uint32_t x[4];
-                stage_load4(pipe.buf(s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x);
+                stage_load4<FULL>(pipe.buf(s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x);
                 a += x[0] + x[1] + x[2] + x[3];
             }
             return block_sum_all<THREADS>(a, s_red);
         }
     }
 
-    template <class P>
+    template <bool FULL, class P>
     __device__ __forceinline__ void finish(const P &pipe, int s, uint32_t tile, uint32_t base,
                                            uint32_t staged, uint32_t n, uint32_t prefix,
-                                           uint32_t agg, bool last) const
+                                           uint32_t agg, bool last, const Carry &) const
     {
         __shared__ uint32_t s_chunk[TT::kChunks];
         const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -224,7 +244,7 @@ struct ScanOp {
         uint32_t lane_excl[ROWS];
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) {
-            stage_load4(pipe.buf(s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x[r]);
+            stage_load4<FULL>(pipe.buf(s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x[r]);
             const uint32_t v = x[r][0] + x[r][1] + x[r][2] + x[r][3];
             uint32_t incl = v;
 #pragma unroll
@@ -247,19 +267,19 @@ struct ScanOp {
                 o[q] = v;
                 v += x[r][q];
             }
-            store4<OUT_VEC>(out, base + r * TT::kRowElems + 4 * tid, n, o);
+            store4<OUT_VEC && !FULL>(out, base + r * TT::kRowElems + 4 * tid, n, o, FULL && OUT_VEC);
         }
         if (tid == 0 && total != nullptr && last) *total = prefix + agg;
         (void)tile;
     }
 
     // float32: each output is hi + (lo + local), with hi + lo the tile's
-    // exclusive prefix (a double split into two floats) and local the float
-    // sum inside the tile.
-    template <class P>
+    // exclusive prefix (a float pair carrying about 48 significant bits) and
+    // local the float sum inside the tile.
+    template <bool FULL, class P>
     __device__ __forceinline__ void finish_f32(const P &pipe, int s, uint32_t base, uint32_t staged,
                                                uint32_t n, float hi, float lo, bool last,
-                                               double inclusive) const
+                                               float inclusive, const Carry &) const
     {
         __shared__ float s_chunk[TT::kChunks];
         const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -267,7 +287,7 @@ struct ScanOp {
         float lane_excl[ROWS];
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) {
-            stage_load4(pipe.buf(s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x[r]);
+            stage_load4<FULL>(pipe.buf(s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x[r]);
             const float v = (__uint_as_float(x[r][0]) + __uint_as_float(x[r][1])) +
                             (__uint_as_float(x[r][2]) + __uint_as_float(x[r][3]));
             float incl = v;
@@ -292,15 +312,15 @@ struct ScanOp {
                 o[q] = __float_as_uint(hi + (lo + local));
                 local += __uint_as_float(x[r][q]);
             }
-            store4<OUT_VEC>(out, base + r * TT::kRowElems + 4 * tid, n, o);
+            store4<OUT_VEC && !FULL>(out, base + r * TT::kRowElems + 4 * tid, n, o, FULL && OUT_VEC);
         }
-        if (tid == 0 && total != nullptr && last) *total = __float_as_uint(float(inclusive));
+        if (tid == 0 && total != nullptr && last) *total = __float_as_uint(inclusive);
     }
 };
 
 // Predicate masks of one staged tile: bit q of mask[r] says element q of
 // thread's vector r is kept (and lies below n).
-template <class TT, class Pred>
+template <class TT, bool FULL, class Pred>
 __device__ __forceinline__ void tile_masks(const uint32_t *sbuf, const uint32_t *gin, uint32_t base,
                                            uint32_t staged, uint32_t n, const Pred &pred,
                                            uint32_t (&x)[TT::kRows][4], uint32_t (&mask)[TT::kRows])
@@ -309,30 +329,39 @@ __device__ __forceinline__ void tile_masks(const uint32_t *sbuf, const uint32_t 
 #pragma unroll
     for (int r = 0; r < TT::kRows; ++r) {
         const uint32_t li = r * TT::kRowElems + 4 * tid;
-        stage_load4(sbuf, gin, base, li, staged, n, 0u, x[r]);
+        stage_load4<FULL>(sbuf, gin, base, li, staged, n, 0u, x[r]);
         uint32_t m = 0u;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) m |= uint32_t(base + li + q < n && pred(x[r][q])) << q;
+        for (int q = 0; q < 4; ++q) m |= uint32_t((FULL || base + li + q < n) && pred(x[r][q])) << q;
         mask[r] = m;
     }
 }
 
-template <class TT, class Pred>
+// Keep count of one staged tile, to every thread; the masks it finds are
+// left in `mask` for the tile's finish a round later.
+template <class TT, bool FULL, class Pred>
 __device__ __forceinline__ uint32_t tile_count(const uint32_t *sbuf, const uint32_t *gin,
                                                uint32_t base, uint32_t staged, uint32_t n,
-                                               const Pred &pred, uint32_t *s_red)
+                                               const Pred &pred, uint32_t *s_red,
+                                               uint32_t (&mask)[TT::kRows])
 {
-    const int tid = threadIdx.x;
+    uint32_t x[TT::kRows][4];
+    tile_masks<TT, FULL>(sbuf, gin, base, staged, n, pred, x, mask);
     uint32_t c = 0u;
 #pragma unroll
-    for (int r = 0; r < TT::kRows; ++r) {
-        const uint32_t li = r * TT::kRowElems + 4 * tid;
-        uint32_t x[4];
-        stage_load4(sbuf, gin, base, li, staged, n, 0u, x);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) c += uint32_t(base + li + q < n && pred(x[q]));
-    }
+    for (int r = 0; r < TT::kRows; ++r) c += __popc(mask[r]);
     return block_sum_all<TT::kThreads>(c, s_red);
+}
+
+// The vectors of one staged tile (no predicate).
+template <class TT, bool FULL>
+__device__ __forceinline__ void tile_vectors(const uint32_t *sbuf, const uint32_t *gin,
+                                             uint32_t base, uint32_t staged, uint32_t n,
+                                             uint32_t (&x)[TT::kRows][4])
+{
+#pragma unroll
+    for (int r = 0; r < TT::kRows; ++r)
+        stage_load4<FULL>(sbuf, gin, base, r * TT::kRowElems + 4 * threadIdx.x, staged, n, 0u, x[r]);
 }
 
 // Stable select-if.  The tile's survivors are compacted in place inside its
@@ -353,23 +382,28 @@ struct SelectOp {
     uint32_t *count;
     Pred pred;
 
-    template <class P>
+    struct Carry {
+        uint32_t mask[ROWS];
+    };
+
+    template <bool FULL, class P>
     __device__ __forceinline__ uint32_t reduce(const P &pipe, int s, uint32_t base, uint32_t staged,
-                                               uint32_t n, uint32_t *s_red) const
+                                               uint32_t n, uint32_t *s_red, Carry &c) const
     {
-        return tile_count<TT>(pipe.buf(s), srcs[0], base, staged, n, pred, s_red);
+        return tile_count<TT, FULL>(pipe.buf(s), srcs[0], base, staged, n, pred, s_red, c.mask);
     }
 
-    template <class P>
+    template <bool FULL, class P>
     __device__ __forceinline__ void finish(const P &pipe, int s, uint32_t tile, uint32_t base,
                                            uint32_t staged, uint32_t n, uint32_t before,
-                                           uint32_t kept, bool last) const
+                                           uint32_t kept, bool last, const Carry &c) const
     {
         __shared__ uint32_t s_chunk[TT::kChunks];
         const int warp = threadIdx.x >> 5;
         uint32_t *buf = pipe.buf(s);
-        uint32_t x[ROWS][4], mask[ROWS], lane_excl[ROWS];
-        tile_masks<TT>(buf, srcs[0], base, staged, n, pred, x, mask);
+        uint32_t x[ROWS][4], lane_excl[ROWS];
+        tile_vectors<TT, FULL>(buf, srcs[0], base, staged, n, x);
+        const uint32_t (&mask)[ROWS] = c.mask;
         rank_masks<TT>(mask, lane_excl, s_chunk);
         __syncthreads();
         if (warp == 0) scan_chunks_warp0<TT>(s_chunk);
@@ -410,30 +444,35 @@ struct PartitionOp {
     uint8_t *ws;
     Pred pred;
 
-    template <class P>
+    struct Carry {
+        uint32_t mask[ROWS];
+    };
+
+    template <bool FULL, class P>
     __device__ __forceinline__ uint32_t reduce(const P &pipe, int s, uint32_t base, uint32_t staged,
-                                               uint32_t n, uint32_t *s_red) const
+                                               uint32_t n, uint32_t *s_red, Carry &c) const
     {
-        return tile_count<TT>(pipe.buf(s), srcs[0], base, staged, n, pred, s_red);
+        return tile_count<TT, FULL>(pipe.buf(s), srcs[0], base, staged, n, pred, s_red, c.mask);
     }
 
-    template <class P>
+    template <bool FULL, class P>
     __device__ __forceinline__ void finish(const P &pipe, int s, uint32_t tile, uint32_t base,
                                            uint32_t staged, uint32_t n, uint32_t before,
-                                           uint32_t kept, bool last) const
+                                           uint32_t kept, bool last, const Carry &c) const
     {
         __shared__ uint32_t s_chunk[TT::kChunks];
         const int tid = threadIdx.x, warp = tid >> 5;
         uint32_t *kbuf = pipe.buf(s, 0);
         uint32_t *vbuf = pipe.buf(s, VALS ? 1 : 0);
-        uint32_t x[ROWS][4], mask[ROWS], lane_excl[ROWS];
+        uint32_t x[ROWS][4], lane_excl[ROWS];
         uint32_t v[VALS ? ROWS : 1][4];
-        tile_masks<TT>(kbuf, srcs[0], base, staged, n, pred, x, mask);
+        tile_vectors<TT, FULL>(kbuf, srcs[0], base, staged, n, x);
+        const uint32_t (&mask)[ROWS] = c.mask;
         if (VALS) {
 #pragma unroll
             for (int r = 0; r < ROWS; ++r)
-                stage_load4(vbuf, srcs[VALS ? 1 : 0], base, r * TT::kRowElems + 4 * tid, staged, n,
-                            0u, v[VALS ? r : 0]);
+                stage_load4<FULL>(vbuf, srcs[VALS ? 1 : 0], base, r * TT::kRowElems + 4 * tid, staged,
+                                  n, 0u, v[VALS ? r : 0]);
         }
         rank_masks<TT>(mask, lane_excl, s_chunk);
         const uint32_t T = *true_total;
@@ -464,7 +503,7 @@ struct PartitionOp {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const uint32_t local = local0 + q;
-                if (base + local < n) {
+                if (FULL || base + local < n) {
                     const bool keep = (mask[r] >> q) & 1u;
                     const uint32_t slot = keep ? sh_kept + ranked : sh_rej + (local - ranked);
                     kbuf[slot] = x[r][q];
