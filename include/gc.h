@@ -187,6 +187,30 @@ gc_status gc_select_if_atomic(const void *d_in, void *d_out, uint32_t *d_count,
                               cudaStream_t stream);
 
 /*
+ * gc_select_if without a workspace, for callers that cannot allocate device
+ * memory where they need the compaction: a plugin whose host framework owns
+ * the device memory budget and forbids allocations behind its back, or a
+ * latency-critical loop that must not pay for cudaMalloc / cudaFree, which
+ * may synchronise the device.  There is no counterpart on the pages this
+ * library follows; the result is exactly gc_select_if's.
+ *
+ * The scratch the kernels need lives in one file-scope device array of
+ * 1,049,600 bytes inside the library, held by every GPU that loads it until
+ * the process exits; it serves n <= GC_NOALLOC_MAX_ELEMENTS (2^28), and
+ * larger n returns GC_ERR_INVALID_VALUE.  The first call on a device (with
+ * that device current) looks up the array's device address and caches it;
+ * make that first call before any stream capture begins.  Every call shares
+ * the array: each clears what must start at zero on its own stream, and
+ * calls that can overlap on the GPU (different streams with no ordering
+ * between them) race on it.  Device-side timeouts of this entry point are
+ * recorded in that array, which no query reads.  No allocation of any kind.
+ */
+#define GC_NOALLOC_MAX_ELEMENTS 268435456u
+gc_status gc_select_if_noalloc(const void *d_in, void *d_out, uint32_t *d_count,
+                               size_t n, gc_dtype dtype, gc_pred pred,
+                               cudaStream_t stream);
+
+/*
  * SYNCHRONOUS.  Waits for `stream`, then reads and clears the device-side
  * error word of the workspace.  Returns GC_OK, GC_ERR_TIMEOUT if a kernel's
  * look-back wait gave up since the last query, GC_ERR_DEVICE_CHECK if a

@@ -220,3 +220,24 @@ def testing_select_if_skip_tile0(x: torch.Tensor, pred, out, count, ws, timeout_
     return int(load().gc_testing_select_if_skip_tile0(
         _ptr(x), _ptr(out), _ptr(count), x.numel(), dtype_code(x), pred_code(pred), _ptr(ws),
         ws.numel(), timeout_ns, _stream(stream)))
+
+
+NOALLOC_MAX_ELEMENTS = 1 << 28
+
+
+def select_if_noalloc(x: torch.Tensor, pred, out: torch.Tensor | None = None,
+                      count: torch.Tensor | None = None, stream=None):
+    """gc_select_if_noalloc: select-if with the library's own fixed scratch
+    (no workspace argument, no allocation by the library).  -> (out, count)."""
+    lib = load()
+    f = lib.gc_select_if_noalloc
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    if out is None:
+        out = torch.empty_like(x)
+    if count is None:
+        count = torch.empty(1, dtype=torch.uint32, device=x.device)
+    _check(f(_ptr(x), _ptr(out), _ptr(count), x.numel(), dtype_code(x), pred_code(pred),
+             _stream(stream)), "gc_select_if_noalloc")
+    return out, count
