@@ -46,7 +46,9 @@ if ROOT not in sys.path:
 from partition_pass_tile_gb300 import synth  # noqa: E402
 
 METRIC = "compaction/scan Gelem/s and achieved HBM GB/s (% of GB300 peak) at n=2^28"
-WORKLOAD = ("stable even/odd partition + select-if sweep (1/50/99 %) at n=2^28 int32, "
+def workload_name(n: int) -> str:
+    size = f"2^{n.bit_length() - 1}" if n & (n - 1) == 0 else str(n)
+    return (f"stable even/odd partition + select-if sweep (1/50/99 %) at n={size} int32, "
             "with exclusive scan (int32, float32), 32-bit one-bit-split LSD radix sort "
             "(uint32 keys + index payload) and the atomic select comparator on the same batch")
 OPS = ["scan_i32", "scan_f32", "select_p01", "select_p50", "select_p99", "partition",
@@ -424,12 +426,13 @@ def run_gc(args):
         "vs_baseline": None,
         "dtype": "int32/uint32/f32",
         "data": "synthetic (seeded SplitMix64)",
-        "config": {"workload": WORKLOAD, "n": n, "bytes_per_array": 4 * n,
+        "config": {"workload": workload_name(n), "n": n, "bytes_per_array": 4 * n,
                    "ops_per_step": OPS, "elements_per_step": elems_step,
                    "alg_bytes_per_step": bytes_step,
                    "alg_gbs": round(bytes_step / ms_step / 1e6, 1),
                    "frac_of_hbm_peak": round(bytes_step / ms_step / 1e6 / peak, 4),
-                   "l2": "inputs 1 GiB each, larger than L2: no flush between steps",
+                   "l2": f"inputs {4 * n / 2**20:.0f} MiB each, larger than the 126 MB L2: "
+                         "no flush between steps",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "ops": ops_report,
         "roofline": {"kernel": "partition_kernel<PredBitClear, payload> (one-bit radix split)",
@@ -437,6 +440,9 @@ def run_gc(args):
                      "peak_kind": f"{peak_kind} hbm_gbs",
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic("split_kernel", n),
+                     "traffic_note": "ncu DRAM read+write bytes of one split launch at n=2^26, "
+                                     "scaled by n/2^26 (profiles/dram_traffic.json); null if "
+                                     "the kernels changed since",
                      "alg_bytes_per_launch": split_bytes,
                      "duration_note": "radix32 call time / 32: includes the histogram pass "
                                       "and each split's status-word clear"},
@@ -479,7 +485,7 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int32/uint32/f64", "data": "synthetic (seeded SplitMix64)",
-        "config": {"workload": WORKLOAD, "n": args.n, "sample_n": sample,
+        "config": {"workload": workload_name(args.n), "n": args.n, "sample_n": sample,
                    "ops_per_step": OPS, "parallelism": "host CPU, one core"},
         "cpu_baseline": {"value": round(value, 4), "unit": "Gelem/s", "kind": "oracle",
                          "cores": 1,

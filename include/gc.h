@@ -178,8 +178,8 @@ gc_status gc_split_radix(const uint32_t *d_keys_in, const uint32_t *d_vals_in,
 /*
  * The atomic-counter comparison path: the same survivors and the same
  * *d_count as gc_select_if, in an order the hardware decides (only the
- * multiset of d_out[0, *d_count) is defined).  One atomic per warp and row
- * of 128 elements on a single counter.
+ * multiset of d_out[0, *d_count) is defined).  One atomic per tile of
+ * gc_tile_elements(GC_OP_SELECT_IF_ATOMIC) elements on a single counter.
  */
 gc_status gc_select_if_atomic(const void *d_in, void *d_out, uint32_t *d_count,
                               size_t n, gc_dtype dtype, gc_pred pred,

@@ -78,41 +78,56 @@ select_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, uint3
 }
 
 // Comparison path ("compaction.cu -- Day 33", compactAtomic): one counter
-// for the whole grid, no scan, no order.  Survivors of one warp and row are
-// counted with a shuffle scan and claim their slots with one atomicAdd;
-// which warp reaches the counter first decides where its run lands.
+// for the whole grid, no scan across tiles, no order between tiles.  Each
+// CTA ranks its tile's survivors (as select_kernel does), claims a run of
+// that many output slots with one atomicAdd on the shared counter, and
+// writes its survivors there; which CTA reaches the counter first decides
+// where its run lands.  One atomic per 4096-element tile instead of one per
+// survivor: the page's version serialises every survivor on one address.
 template <class Pred, int THREADS, int ROWS, bool VEC>
 __global__ void __launch_bounds__(THREADS)
 select_atomic_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out,
                      uint32_t *count, uint32_t n, Pred pred)
 {
     using TT = Tile<THREADS, ROWS>;
-    const int tid = threadIdx.x, lane = tid & 31;
+    __shared__ uint32_t s_chunk[TT::kChunks];
+    __shared__ uint32_t s_base, s_kept;
+    __shared__ __align__(16) uint32_t s_buf[TT::kElems + 4];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t base = blockIdx.x * uint32_t(TT::kElems);
+
+    uint32_t x[ROWS][4], mask[ROWS], lane_excl[ROWS];
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
         const uint32_t idx = base + r * TT::kRowElems + 4 * tid;
-        uint32_t x[4];
-        load4<VEC>(in, idx, n, 0u, x);
+        load4<VEC>(in, idx, n, 0u, x[r]);
         uint32_t m = 0u;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) m |= uint32_t(idx + k < n && pred(x[k])) << k;
-        const uint32_t c = __popc(m);
-        uint32_t incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(kFullMask, incl, o);
-            if (lane >= o) incl += y;
+        for (int k = 0; k < 4; ++k) m |= uint32_t(idx + k < n && pred(x[r][k])) << k;
+        mask[r] = m;
+    }
+    rank_masks<TT>(mask, lane_excl, s_chunk);
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t kept = scan_chunks_warp0<TT>(s_chunk);
+        if (lane == 0) {
+            s_kept = kept;
+            s_base = kept != 0u ? atomicAdd(count, kept) : 0u;
         }
-        const uint32_t warp_total = __shfl_sync(kFullMask, incl, 31);
-        if (warp_total == 0u) continue;
-        uint32_t slot = 0u;
-        if (lane == 31) slot = atomicAdd(count, warp_total);
-        slot = __shfl_sync(kFullMask, slot, 31) + incl - c;
+    }
+    __syncthreads();
+    const uint32_t kept = s_kept, out_base = s_base;
+    if (kept == 0u) return;
+    const uint32_t shift = VEC ? (out_base & 3u) : 0u;
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        uint32_t pos = shift + s_chunk[r * TT::kWarps + warp] + lane_excl[r];
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            if ((m >> k) & 1u) out[slot++] = x[k];
+            if ((mask[r] >> k) & 1u) s_buf[pos++] = x[r][k];
     }
+    __syncthreads();
+    store_run<THREADS, VEC>(out, out_base, s_buf, shift, kept);
 }
 
 template <class Pred>
@@ -154,7 +169,7 @@ cudaError_t dispatch_atomic(const uint32_t *in, uint32_t *out, uint32_t *count, 
     const uint32_t tiles = uint32_t(gch::ceil_div(n, gch::tile_elems(T, R)));
     cudaError_t e = cudaMemsetAsync(count, 0, sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
-    if (gch::aligned16(in))
+    if (gch::aligned16(in) && gch::aligned16(out))
         select_atomic_kernel<Pred, T, R, true><<<tiles, T, 0, s>>>(in, out, count, n, pred);
     else
         select_atomic_kernel<Pred, T, R, false><<<tiles, T, 0, s>>>(in, out, count, n, pred);
