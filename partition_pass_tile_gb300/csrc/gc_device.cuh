@@ -289,8 +289,9 @@ struct Tile {
     static constexpr int kElems = kRowElems * ROWS;
     static constexpr int kChunks = kWarps * ROWS;
     static_assert(THREADS % 32 == 0, "whole warps");
-    static_assert(kChunks % 32 == 0, "chunk totals are scanned 32 at a time by one warp");
-    static constexpr int kChunksPerLane = kChunks / 32;
+    static_assert(kChunks % 32 == 0 || (kChunks < 32 && 32 % kChunks == 0),
+                  "chunk totals are scanned by one warp: a multiple of 32, or fewer");
+    static constexpr int kChunksPerLane = kChunks >= 32 ? kChunks / 32 : 1;
 };
 
 // Loads the 4 elements at [idx, idx + 4) into v; elements at or past n get
@@ -338,11 +339,13 @@ __device__ __forceinline__ V scan_chunks_warp0(V *s_chunk)
 {
     const int lane = threadIdx.x & 31;
     constexpr int K = TileT::kChunksPerLane;
+    // with fewer than 32 chunks the lanes past the last one carry zeros
+    constexpr bool kShort = TileT::kChunks < 32;
     V c[K];
     V run = V(0);
 #pragma unroll
     for (int k = 0; k < K; ++k) {
-        c[k] = s_chunk[lane * K + k];
+        c[k] = (!kShort || lane < TileT::kChunks) ? s_chunk[lane * K + k] : V(0);
         run += c[k];
     }
     V incl = run;
@@ -356,7 +359,7 @@ __device__ __forceinline__ V scan_chunks_warp0(V *s_chunk)
     if (lane == 0) excl = V(0);
 #pragma unroll
     for (int k = 0; k < K; ++k) {
-        s_chunk[lane * K + k] = excl;
+        if (!kShort || lane < TileT::kChunks) s_chunk[lane * K + k] = excl;
         excl += c[k];
     }
     return total;
@@ -778,6 +781,47 @@ __device__ __forceinline__ V block_sum_all(V v, V *s_red)
 #pragma unroll
     for (int w = 0; w < THREADS / 32; ++w) t += s_red[w];
     return t;
+}
+
+// ---------------------------------------------------------------- chunk offsets
+// Every warp computes the exclusive scan of the tile's kChunks chunk totals
+// (in s_chunk, chunk c = row * WARPS + warp) by itself and keeps the offsets
+// of its own chunks, one per row, plus the tile total: one barrier (before
+// the call) serves both the tile's reduction and its ranking.
+template <class TT, class V>
+__device__ __forceinline__ void chunk_offsets(const V *s_chunk, V (&off)[TT::kRows], V &total)
+{
+    constexpr int K = TT::kChunksPerLane;
+    constexpr bool kShort = TT::kChunks < 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    V c[K];
+    V run = V(0);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        c[k] = (!kShort || lane < TT::kChunks) ? s_chunk[lane * K + k] : V(0);
+        run += c[k];
+    }
+    V incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const V y = __shfl_up_sync(kFullMask, incl, o);
+        if (lane >= o) incl += y;
+    }
+    total = __shfl_sync(kFullMask, incl, 31);
+    V e[K];
+    e[0] = __shfl_up_sync(kFullMask, incl, 1);
+    if (lane == 0) e[0] = V(0);
+#pragma unroll
+    for (int k = 1; k < K; ++k) e[k] = e[k - 1] + c[k - 1];
+#pragma unroll
+    for (int r = 0; r < TT::kRows; ++r) {
+        const int ch = r * TT::kWarps + warp;  // warp-uniform
+        V mine = e[0];
+#pragma unroll
+        for (int k = 1; k < K; ++k)
+            if (ch % K == k) mine = e[k];
+        off[r] = __shfl_sync(kFullMask, mine, ch / K);
+    }
 }
 
 }  // namespace gcd

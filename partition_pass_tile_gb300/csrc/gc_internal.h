@@ -91,6 +91,7 @@ constexpr int kPartPipeStages = GC_PART_PIPE_STAGES;
 constexpr int kSplitPipeThreads = GC_SPLIT_PIPE_THREADS, kSplitPipeRows = GC_SPLIT_PIPE_ROWS;
 constexpr int kSplitPipeStages = GC_SPLIT_PIPE_STAGES;
 
+
 constexpr int kScanThreads = GC_SCAN_THREADS, kScanRows = GC_SCAN_ROWS;
 constexpr int kSelectThreads = GC_SELECT_THREADS, kSelectRows = GC_SELECT_ROWS;
 constexpr int kPartThreads = GC_PART_THREADS, kPartRows = GC_PART_ROWS;

@@ -32,6 +32,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 
 #include "gc_device.cuh"
 #include "gc_pipe.cuh"
@@ -102,6 +103,18 @@ __device__ __forceinline__ void window_finish_ff(const uint64_t *status, uint32_
 }
 
 // ---------------------------------------------------------------- the driver
+//
+// Per iteration (t = this CTA's k-th tile, p = its previous one):
+//   window loads for p issued;
+//   op.reduce(t): predicate / sums, in-tile ranks, one barrier, then every
+//     warp derives the tile total and its own chunk offsets; the aggregate is
+//     published and the per-thread offsets (and masks) are carried to t's
+//     finish one iteration later;
+//   op.load(p): p's elements into registers;
+//   window finish (one barrier, which also orders every read of p's stage
+//     before the writes op.finish may make into it);
+//   op.finish(p): outputs from the carried offsets;
+//   a barrier, then p's stage is re-armed.
 template <int THREADS, int STAGES, class Op>
 __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32_t n,
                                              uint32_t num_tiles, uint8_t *ws, uint64_t timeout_ns)
@@ -110,7 +123,6 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
     using P = typename Op::template PipeT<STAGES>;
     constexpr uint32_t TE = Op::kTileElems;
     constexpr int W = THREADS / 32;
-    __shared__ uint32_t s_red[W];
     __shared__ uint32_t s_win_u[W];
     __shared__ float s_win_hi[W], s_win_lo[W];
     const P pipe{smem};
@@ -141,9 +153,9 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
             const uint32_t base = tile * TE;
             const uint32_t staged = staged_elems(tile, TE, n);
             if (staged == TE)
-                agg = op.template reduce<true>(pipe, s, base, staged, n, s_red, cur);
+                agg = op.template reduce<true>(pipe, s, base, staged, n, cur);
             else
-                agg = op.template reduce<false>(pipe, s, base, staged, n, s_red, cur);
+                agg = op.template reduce<false>(pipe, s, base, staged, n, cur);
             if (tid == 0) publish_aggregate(status, tile, agg);
         }
 
@@ -151,7 +163,15 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
             const int ps = int((k - 1) % STAGES);
             const uint32_t pbase = prev * TE;
             const uint32_t pstaged = staged_elems(prev, TE, n);
+            const bool full = pstaged == TE;
             const bool last = prev == num_tiles - 1;
+            typename Op::Loaded ld;
+            if constexpr (Op::kPreload) {
+                if (full)
+                    op.template load<true>(pipe, ps, pbase, pstaged, n, ld);
+                else
+                    op.template load<false>(pipe, ps, pbase, pstaged, n, ld);
+            }
             if constexpr (Op::kF32) {
                 float wh, wl_;
                 window_finish_ff<THREADS>(status, window_lo(prev), prev, wl, ws, prev, timeout_ns,
@@ -159,10 +179,10 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
                 float ph, pl;
                 ff_add(run_h, run_l, wh, wl_, ph, pl);  // prefix(p) = run + window
                 ff_add(ph, pl, __uint_as_float(prev_agg), 0.0f, run_h, run_l);
-                if (pstaged == TE)
-                    op.template finish_f32<true>(pipe, ps, pbase, pstaged, n, ph, pl, last, run_h + run_l, prv);
+                if (full)
+                    op.template finish_f32<true>(pipe, ps, pbase, pstaged, n, ph, pl, last, run_h + run_l, prv, ld);
                 else
-                    op.template finish_f32<false>(pipe, ps, pbase, pstaged, n, ph, pl, last, run_h + run_l, prv);
+                    op.template finish_f32<false>(pipe, ps, pbase, pstaged, n, ph, pl, last, run_h + run_l, prv, ld);
             } else {
                 uint32_t wsum_u;
                 double unused;
@@ -170,10 +190,10 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
                                               s_win_u, nullptr, wsum_u, unused);
                 const uint32_t prefix = run_u + wsum_u;
                 run_u = prefix + prev_agg;
-                if (pstaged == TE)
-                    op.template finish<true>(pipe, ps, prev, pbase, pstaged, n, prefix, prev_agg, last, prv);
+                if (full)
+                    op.template finish<true>(pipe, ps, prev, pbase, pstaged, n, prefix, prev_agg, last, prv, ld);
                 else
-                    op.template finish<false>(pipe, ps, prev, pbase, pstaged, n, prefix, prev_agg, last, prv);
+                    op.template finish<false>(pipe, ps, prev, pbase, pstaged, n, prefix, prev_agg, last, prv, ld);
             }
             __syncthreads();  // the previous tile's stage is free again
             if (tid == 0) pipe.refill(ps, op.srcs, prev, TE, n, num_tiles);
@@ -191,6 +211,17 @@ constexpr int pipeline_max_grid() { return kWinPerThread * THREADS + 1; }
 
 // ---------------------------------------------------------------- tile bodies
 
+// The vectors of one staged tile.
+template <class TT, bool FULL>
+__device__ __forceinline__ void tile_vectors(const uint32_t *sbuf, const uint32_t *gin,
+                                             uint32_t base, uint32_t staged, uint32_t n,
+                                             uint32_t (&x)[TT::kRows][4])
+{
+#pragma unroll
+    for (int r = 0; r < TT::kRows; ++r)
+        stage_load4<FULL>(sbuf, gin, base, r * TT::kRowElems + 4 * threadIdx.x, staged, n, 0u, x[r]);
+}
+
 // Exclusive scan, uint32 (int32 bits) or float32.
 template <int THREADS, int ROWS, bool F32, bool OUT_VEC>
 struct ScanOp {
@@ -205,11 +236,18 @@ struct ScanOp {
     uint32_t *total;
 
     struct Carry {};
+    static constexpr bool kPreload = false;
+    struct Loaded {};
 
     template <bool FULL, class P>
+    __device__ __forceinline__ void load(const P &, int, uint32_t, uint32_t, uint32_t, Loaded &) const {}
+
+    // The aggregate only: a plain sum, so it is published as early as possible.
+    template <bool FULL, class P>
     __device__ __forceinline__ uint32_t reduce(const P &pipe, int s, uint32_t base, uint32_t staged,
-                                               uint32_t n, uint32_t *s_red, Carry &) const
+                                               uint32_t n, Carry &) const
     {
+        __shared__ uint32_t s_red[TT::kWarps];
         const int tid = threadIdx.x;
         if constexpr (F32) {
             float a = 0.0f;
@@ -236,7 +274,8 @@ struct ScanOp {
     template <bool FULL, class P>
     __device__ __forceinline__ void finish(const P &pipe, int s, uint32_t tile, uint32_t base,
                                            uint32_t staged, uint32_t n, uint32_t prefix,
-                                           uint32_t agg, bool last, const Carry &) const
+                                           uint32_t agg, bool last, const Carry &,
+                                           const Loaded &) const
     {
         __shared__ uint32_t s_chunk[TT::kChunks];
         const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -279,7 +318,7 @@ struct ScanOp {
     template <bool FULL, class P>
     __device__ __forceinline__ void finish_f32(const P &pipe, int s, uint32_t base, uint32_t staged,
                                                uint32_t n, float hi, float lo, bool last,
-                                               float inclusive, const Carry &) const
+                                               float inclusive, const Carry &, const Loaded &) const
     {
         __shared__ float s_chunk[TT::kChunks];
         const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -319,9 +358,113 @@ struct ScanOp {
 };
 
 // Predicate masks of one staged tile: bit q of mask[r] says element q of
-// thread's vector r is kept (and lies below n).
+// the thread's vector r is kept (and lies below n).
 template <class TT, bool FULL, class Pred>
 __device__ __forceinline__ void tile_masks(const uint32_t *sbuf, const uint32_t *gin, uint32_t base,
+                                           uint32_t staged, uint32_t n, const Pred &pred,
+                                           uint32_t (&mask)[TT::kRows])
+{
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int r = 0; r < TT::kRows; ++r) {
+        const uint32_t li = r * TT::kRowElems + 4 * tid;
+        uint32_t x[4];
+        stage_load4<FULL>(sbuf, gin, base, li, staged, n, 0u, x);
+        uint32_t m = 0u;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) m |= uint32_t((FULL || base + li + q < n) && pred(x[q])) << q;
+        mask[r] = m;
+    }
+}
+
+// Reduction of a predicate tile: masks, in-tile ranks and the keep count.
+// base[r] = survivors of the tile before this thread's vector r.
+template <class TT, bool FULL, class Pred>
+__device__ __forceinline__ uint32_t rank_tile(const uint32_t *sbuf, const uint32_t *gin,
+                                              uint32_t base, uint32_t staged, uint32_t n,
+                                              const Pred &pred, uint32_t (&mask)[TT::kRows],
+                                              uint32_t (&rbase)[TT::kRows])
+{
+    __shared__ uint32_t s_chunk[TT::kChunks];
+    tile_masks<TT, FULL>(sbuf, gin, base, staged, n, pred, mask);
+    uint32_t lane_excl[TT::kRows];
+    rank_masks<TT>(mask, lane_excl, s_chunk);
+    __syncthreads();
+    uint32_t off[TT::kRows], kept;
+    chunk_offsets<TT>(s_chunk, off, kept);
+#pragma unroll
+    for (int r = 0; r < TT::kRows; ++r) rbase[r] = off[r] + lane_excl[r];
+    return kept;
+}
+
+// Stable select-if.  The tile's survivors are compacted in place inside its
+// own stage buffer (every element was read into registers before the barrier
+// that precedes the first write, and a survivor's rank never exceeds its
+// index), shifted so that shared and global addresses agree modulo 16 bytes,
+// then written as one contiguous run with 128-bit stores.
+template <int THREADS, int ROWS, class Pred, bool VEC>
+struct SelectOp {
+    using TT = Tile<THREADS, ROWS>;
+    static constexpr uint32_t kTileElems = TT::kElems;
+    static constexpr bool kF32 = false;
+    template <int STAGES>
+    using PipeT = Pipe<kTileElems * 4u, STAGES, 1>;
+
+    const uint32_t *srcs[1];
+    uint32_t *out;
+    uint32_t *count;
+    Pred pred;
+
+    struct Carry {
+        uint32_t mask[ROWS];
+        uint32_t base[ROWS];
+    };
+    // The tile is read into registers before the window barrier, which then
+    // also orders those reads before the in-place compaction's writes.
+    static constexpr bool kPreload = true;
+    struct Loaded {
+        uint32_t x[ROWS][4];
+    };
+
+    template <bool FULL, class P>
+    __device__ __forceinline__ uint32_t reduce(const P &pipe, int s, uint32_t base, uint32_t staged,
+                                               uint32_t n, Carry &c) const
+    {
+        return rank_tile<TT, FULL>(pipe.buf(s), srcs[0], base, staged, n, pred, c.mask, c.base);
+    }
+
+    template <bool FULL, class P>
+    __device__ __forceinline__ void load(const P &pipe, int s, uint32_t base, uint32_t staged,
+                                         uint32_t n, Loaded &ld) const
+    {
+        tile_vectors<TT, FULL>(pipe.buf(s), srcs[0], base, staged, n, ld.x);
+    }
+
+    template <bool FULL, class P>
+    __device__ __forceinline__ void finish(const P &pipe, int s, uint32_t tile, uint32_t, uint32_t,
+                                           uint32_t, uint32_t before, uint32_t kept, bool last,
+                                           const Carry &c, const Loaded &ld) const
+    {
+        uint32_t *buf = pipe.buf(s);
+        const uint32_t shift = VEC ? (before & 3u) : 0u;
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            uint32_t pos = shift + c.base[r];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if ((c.mask[r] >> q) & 1u) buf[pos++] = ld.x[r][q];
+        }
+        __syncthreads();
+        store_run<THREADS, VEC>(out, before, buf, shift, kept);
+        if (threadIdx.x == 0 && last) *count = before + kept;
+        (void)tile;
+    }
+};
+
+// Predicate masks of one staged tile: bit q of mask[r] says element q of
+// thread's vector r is kept (and lies below n).
+template <class TT, bool FULL, class Pred>
+__device__ __forceinline__ void tile_masks_x(const uint32_t *sbuf, const uint32_t *gin, uint32_t base,
                                            uint32_t staged, uint32_t n, const Pred &pred,
                                            uint32_t (&x)[TT::kRows][4], uint32_t (&mask)[TT::kRows])
 {
@@ -346,82 +489,12 @@ __device__ __forceinline__ uint32_t tile_count(const uint32_t *sbuf, const uint3
                                                uint32_t (&mask)[TT::kRows])
 {
     uint32_t x[TT::kRows][4];
-    tile_masks<TT, FULL>(sbuf, gin, base, staged, n, pred, x, mask);
+    tile_masks_x<TT, FULL>(sbuf, gin, base, staged, n, pred, x, mask);
     uint32_t c = 0u;
 #pragma unroll
     for (int r = 0; r < TT::kRows; ++r) c += __popc(mask[r]);
     return block_sum_all<TT::kThreads>(c, s_red);
 }
-
-// The vectors of one staged tile (no predicate).
-template <class TT, bool FULL>
-__device__ __forceinline__ void tile_vectors(const uint32_t *sbuf, const uint32_t *gin,
-                                             uint32_t base, uint32_t staged, uint32_t n,
-                                             uint32_t (&x)[TT::kRows][4])
-{
-#pragma unroll
-    for (int r = 0; r < TT::kRows; ++r)
-        stage_load4<FULL>(sbuf, gin, base, r * TT::kRowElems + 4 * threadIdx.x, staged, n, 0u, x[r]);
-}
-
-// Stable select-if.  The tile's survivors are compacted in place inside its
-// own stage buffer (every element is read into registers before the barrier
-// that precedes the first write, and a survivor's rank never exceeds its
-// index), shifted so that shared and global addresses agree modulo 16 bytes,
-// then written as one contiguous run with 128-bit stores.
-template <int THREADS, int ROWS, class Pred, bool VEC>
-struct SelectOp {
-    using TT = Tile<THREADS, ROWS>;
-    static constexpr uint32_t kTileElems = TT::kElems;
-    static constexpr bool kF32 = false;
-    template <int STAGES>
-    using PipeT = Pipe<kTileElems * 4u, STAGES, 1>;
-
-    const uint32_t *srcs[1];
-    uint32_t *out;
-    uint32_t *count;
-    Pred pred;
-
-    struct Carry {
-        uint32_t mask[ROWS];
-    };
-
-    template <bool FULL, class P>
-    __device__ __forceinline__ uint32_t reduce(const P &pipe, int s, uint32_t base, uint32_t staged,
-                                               uint32_t n, uint32_t *s_red, Carry &c) const
-    {
-        return tile_count<TT, FULL>(pipe.buf(s), srcs[0], base, staged, n, pred, s_red, c.mask);
-    }
-
-    template <bool FULL, class P>
-    __device__ __forceinline__ void finish(const P &pipe, int s, uint32_t tile, uint32_t base,
-                                           uint32_t staged, uint32_t n, uint32_t before,
-                                           uint32_t kept, bool last, const Carry &c) const
-    {
-        __shared__ uint32_t s_chunk[TT::kChunks];
-        const int warp = threadIdx.x >> 5;
-        uint32_t *buf = pipe.buf(s);
-        uint32_t x[ROWS][4], lane_excl[ROWS];
-        tile_vectors<TT, FULL>(buf, srcs[0], base, staged, n, x);
-        const uint32_t (&mask)[ROWS] = c.mask;
-        rank_masks<TT>(mask, lane_excl, s_chunk);
-        __syncthreads();
-        if (warp == 0) scan_chunks_warp0<TT>(s_chunk);
-        __syncthreads();
-        const uint32_t shift = VEC ? (before & 3u) : 0u;
-#pragma unroll
-        for (int r = 0; r < ROWS; ++r) {
-            uint32_t pos = shift + s_chunk[r * TT::kWarps + warp] + lane_excl[r];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if ((mask[r] >> q) & 1u) buf[pos++] = x[r][q];
-        }
-        __syncthreads();
-        store_run<THREADS, VEC>(out, before, buf, shift, kept);
-        if (threadIdx.x == 0 && last) *count = before + kept;
-        (void)tile;
-    }
-};
 
 // Stable partition (and the radix one-bit split, with payloads): kept
 // elements go to [before, before + kept) and rejected ones to
@@ -447,18 +520,25 @@ struct PartitionOp {
     struct Carry {
         uint32_t mask[ROWS];
     };
+    static constexpr bool kPreload = false;
+    struct Loaded {};
+
+    template <bool FULL, class P>
+    __device__ __forceinline__ void load(const P &, int, uint32_t, uint32_t, uint32_t, Loaded &) const {}
 
     template <bool FULL, class P>
     __device__ __forceinline__ uint32_t reduce(const P &pipe, int s, uint32_t base, uint32_t staged,
-                                               uint32_t n, uint32_t *s_red, Carry &c) const
+                                               uint32_t n, Carry &c) const
     {
+        __shared__ uint32_t s_red[TT::kWarps];
         return tile_count<TT, FULL>(pipe.buf(s), srcs[0], base, staged, n, pred, s_red, c.mask);
     }
 
     template <bool FULL, class P>
     __device__ __forceinline__ void finish(const P &pipe, int s, uint32_t tile, uint32_t base,
                                            uint32_t staged, uint32_t n, uint32_t before,
-                                           uint32_t kept, bool last, const Carry &c) const
+                                           uint32_t kept, bool last, const Carry &c,
+                                           const Loaded &) const
     {
         __shared__ uint32_t s_chunk[TT::kChunks];
         const int tid = threadIdx.x, warp = tid >> 5;
