@@ -363,41 +363,101 @@ def run_gc(args):
     op_ms = {name: sum(e[name][0].elapsed_time(e[name][1]) for e in evs) / args.steps
              for name in OPS}
 
-    # end to end: pinned host inputs in, outputs and counts back, every step
+    # End to end: every step copies its inputs in from pinned host memory and
+    # every output (and the counts) back, through the C ABI.  Three streams:
+    # host-to-device copies, the kernels, device-to-host copies, ordered by
+    # events.  Device inputs are double-buffered by step parity, so the copies
+    # of step k + 1 run while step k computes; each op has its own device
+    # output, copied back while the next op runs.
     pinned = {k: torch.from_numpy(v.view(np.int32) if v.dtype == np.uint32 else v).pin_memory()
               for k, v in h.items()}
-    host_out = torch.empty(n, dtype=torch.int32).pin_memory()
-    host_out_b = torch.empty(n, dtype=torch.int32).pin_memory()
+    d_in = [d, {k: torch.empty_like(v) for k, v in d.items()}]
+    outs = {name: torch.empty(n, dtype=torch.int32, device=dev) for name in OPS}
+    out_vals = torch.empty(n, dtype=torch.int32, device=dev)
+    host_outs = {name: torch.empty(n, dtype=torch.int32).pin_memory() for name in OPS}
+    host_vals = torch.empty(n, dtype=torch.int32).pin_memory()
     host_counts = torch.empty(8, dtype=torch.int32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
-    d2h_per_op = {"radix32": 2 * 4 * n}
-    d2h = sum(d2h_per_op.get(k, 4 * n) for k in OPS) + host_counts.numel() * 4
+    d2h = sum(4 * n for _ in OPS) + 4 * n + host_counts.numel() * 4
+    s_h2d = torch.cuda.Stream(device=dev)
+    s_d2h = torch.cuda.Stream(device=dev)
+    inputs_of = {"scan_i32": ["x"], "scan_f32": ["f"], "select_p01": ["s01"],
+                 "select_p50": ["s50"], "select_p99": ["s99"], "partition": ["x"],
+                 "radix32": ["x", "payload"], "atomic_p50": ["s50"]}
+    set_free = [None, None]  # event: the compute stream is done with an input set
+    out_free = {name: None for name in OPS}  # event: an op's output has been copied back
 
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            for k, v in pinned.items():
-                dst = d[k].view(torch.int32) if d[k].dtype == torch.uint32 else d[k]
+    def e2e_ops(dd):
+        xk = dd["x"].view(torch.uint32)
+        o = outs
+        return {
+            "scan_i32": lambda: gc.exclusive_scan(dd["x"], out=o["scan_i32"], total=counts[0:1].view(torch.int32), ws=ws, stream=stream),
+            "scan_f32": lambda: gc.exclusive_scan(dd["f"], out=o["scan_f32"].view(torch.float32), total=counts[1:2].view(torch.float32), ws=ws, stream=stream),
+            "select_p01": lambda: gc.select_if(dd["s01"], "nonzero", out=o["select_p01"], count=counts[2:3], ws=ws, stream=stream),
+            "select_p50": lambda: gc.select_if(dd["s50"], "nonzero", out=o["select_p50"], count=counts[3:4], ws=ws, stream=stream),
+            "select_p99": lambda: gc.select_if(dd["s99"], "nonzero", out=o["select_p99"], count=counts[4:5], ws=ws, stream=stream),
+            "partition": lambda: gc.partition(dd["x"], "even", out=o["partition"], count_true=counts[5:6], ws=ws, stream=stream),
+            "radix32": lambda: gc.split_radix(xk, dd["payload"], 0, 32, keys_out=o["radix32"].view(torch.uint32),
+                                              vals_out=out_vals.view(torch.uint32), ws=ws, stream=stream),
+            "atomic_p50": lambda: gc.select_if_atomic(dd["s50"], "nonzero", out=o["atomic_p50"], count=counts[7:8], ws=ws, stream=stream),
+        }
+
+    def e2e_step(k):
+        par = k % 2
+        dd = d_in[par]
+        arrived = {}
+        if set_free[par] is not None:
+            s_h2d.wait_event(set_free[par])
+        for key, v in pinned.items():
+            dst = dd[key].view(torch.int32) if dd[key].dtype == torch.uint32 else dd[key]
+            with torch.cuda.stream(s_h2d):
                 dst.copy_(v, non_blocking=True)
-            for name, fn in op_calls():
-                fn()
-                host_out.copy_(out_a, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(s_h2d)
+            arrived[key] = ev
+        calls = e2e_ops(dd)
+        for name in OPS:
+            for key in inputs_of[name]:
+                stream.wait_event(arrived[key])
+            if out_free[name] is not None:
+                stream.wait_event(out_free[name])
+            calls[name]()
+            done = torch.cuda.Event()
+            done.record(stream)
+            s_d2h.wait_event(done)
+            with torch.cuda.stream(s_d2h):
+                host_outs[name].copy_(outs[name], non_blocking=True)
                 if name == "radix32":
-                    host_out_b.copy_(out_b, non_blocking=True)
+                    host_vals.copy_(out_vals, non_blocking=True)
+            freed = torch.cuda.Event()
+            freed.record(s_d2h)
+            out_free[name] = freed
+        consumed = torch.cuda.Event()
+        consumed.record(stream)
+        set_free[par] = consumed
+        s_d2h.wait_event(consumed)
+        with torch.cuda.stream(s_d2h):
             host_counts.copy_(counts.view(torch.int32), non_blocking=True)
 
-    e2e_step()
-    stream.synchronize()
+    e2e_step(0)
+    e2e_step(1)
+    torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_h2d)
+    stream.wait_event(e0)
+    s_d2h.wait_event(e0)
+    for k in range(args.steps):
+        e2e_step(k)
+    e1.record(s_d2h)  # the last copy back depends on every copy in and every kernel
     torch.cuda.synchronize(dev)
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
+    # the copied-back counts are the true ones (the step really ran)
+    hc = host_counts.numpy().view(np.uint32)
+    assert int(hc[3]) == kept["select_p50"] and int(hc[7]) == kept["atomic_p50"]
 
     peak, peak_kind = read_peaks()
     elems_step = len(OPS) * n
@@ -450,7 +510,9 @@ def run_gc(args):
         "e2e": {"value": round(sum_over_ranks(elems_step, world, dev) / (e2e_ms / 1e3) / 1e9, 3),
                 "unit": "Gelem/s", "ms_per_step": round(e2e_ms, 3),
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "path": "pinned host buffers -> H2D -> gc_* through the C ABI -> D2H of every output"},
+                "path": "pinned host inputs -> H2D (own stream, inputs double-buffered by step) -> "
+                        "gc_* through the C ABI -> D2H of every output and the counts (own "
+                        "stream), every step"},
         "gpu_launches": sum(LAUNCHES_PER_OP.values()) * args.steps,
     }
     if rank == 0:
