@@ -23,6 +23,9 @@ Parity status of each function (what pins it, in ``tests/test_oracle_pins.py``):
   invariants, the i - rank[i] identity.
 * split_radix: numpy's stable argsort (a library routine) on keys, payload
   permutation, single-bit case against partition.
+* select_if_cmp / partition_cmp: numpy's element-wise comparisons and
+  masked-bit tests (library routines, IEEE semantics for float32) on inputs
+  with every float special value; the fixed predicates as special cases.
 """
 
 from __future__ import annotations
@@ -36,6 +39,7 @@ import numpy as np
 
 I32, U32, F32 = 0, 1, 2
 NONZERO, ODD, EVEN = 0, 1, 2
+LT, LE, GT, GE, EQ, NE, MASK_EQ, MASK_NE = range(8)
 
 _HERE = Path(__file__).resolve().parent
 _SRC = _HERE / "oracle.c"
@@ -84,6 +88,11 @@ def load_library(path: str | os.PathLike | None = None) -> ctypes.CDLL:
     lib.orc_partition.restype = Z
     lib.orc_split_radix.argtypes = [P, P, P, P, Z, I, I]
     lib.orc_split_radix.restype = I
+    U = ctypes.c_uint32
+    lib.orc_select_if_cmp.argtypes = [P, P, Z, I, I, U, U]
+    lib.orc_select_if_cmp.restype = Z
+    lib.orc_partition_cmp.argtypes = [P, P, Z, I, I, U, U]
+    lib.orc_partition_cmp.restype = Z
     lib.orc_count_out_of_order.argtypes = [P, P, Z]
     lib.orc_count_out_of_order.restype = Z
     return lib
@@ -162,6 +171,28 @@ class Oracle:
         x = _c(x)
         out = np.empty_like(x)
         t = self.lib.orc_partition(_ptr(x), _ptr(out), x.shape[0], _dtype_code(x), pred)
+        return out, int(t)
+
+    @staticmethod
+    def operand_bits(x: np.ndarray, value) -> int:
+        """The 32-bit pattern of `value` in x's dtype."""
+        return int(np.array([value], dtype=x.dtype).view(np.uint32)[0])
+
+    def select_if_cmp(self, x: np.ndarray, cmp: int, value=0, mask: int = 0) -> np.ndarray:
+        """value: a number of x's dtype for LT..NE, a raw 32-bit pattern for MASK_*."""
+        x = _c(x)
+        out = np.empty_like(x)
+        v = int(value) & 0xFFFFFFFF if cmp >= MASK_EQ else self.operand_bits(x, value)
+        m = self.lib.orc_select_if_cmp(_ptr(x), _ptr(out), x.shape[0], _dtype_code(x), cmp, v,
+                                       mask & 0xFFFFFFFF)
+        return out[:m].copy()
+
+    def partition_cmp(self, x: np.ndarray, cmp: int, value=0, mask: int = 0):
+        x = _c(x)
+        out = np.empty_like(x)
+        v = int(value) & 0xFFFFFFFF if cmp >= MASK_EQ else self.operand_bits(x, value)
+        t = self.lib.orc_partition_cmp(_ptr(x), _ptr(out), x.shape[0], _dtype_code(x), cmp, v,
+                                       mask & 0xFFFFFFFF)
         return out, int(t)
 
     def split_radix(self, keys: np.ndarray, vals: np.ndarray | None = None,

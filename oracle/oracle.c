@@ -255,6 +255,90 @@ int orc_split_radix(const uint32_t *keys_in, const uint32_t *vals_in,
 }
 
 /*
+ * Parameterised predicates ("The CUDA Handbook, ch. 13: Stream compaction":
+ * the single-pass compaction "is easily modified to evaluate more-complicated
+ * predicates").  Either a comparison of the element with an operand in the
+ * dtype's own order -- int32 signed, uint32 unsigned, float32 IEEE 754, where
+ * every comparison with NaN is false except "not equal" -- or a test of the
+ * raw bits under a mask.  value holds the operand's 32-bit pattern.
+ */
+enum { ORC_LT = 0, ORC_LE = 1, ORC_GT = 2, ORC_GE = 3, ORC_EQ = 4, ORC_NE = 5,
+       ORC_MASK_EQ = 6, ORC_MASK_NE = 7 };
+
+static int keep_cmp(uint32_t bits, int dtype, int cmp, uint32_t value, uint32_t mask)
+{
+    if (cmp == ORC_MASK_EQ) return (bits & mask) == value;
+    if (cmp == ORC_MASK_NE) return (bits & mask) != value;
+    if (dtype == ORC_F32) {
+        const float x = bits_to_float(bits), v = bits_to_float(value);
+        switch (cmp) {
+        case ORC_LT: return x < v;
+        case ORC_LE: return x <= v;
+        case ORC_GT: return x > v;
+        case ORC_GE: return x >= v;
+        case ORC_EQ: return x == v;
+        default: return x != v;
+        }
+    }
+    if (dtype == ORC_I32) {
+        int32_t x, v;
+        memcpy(&x, &bits, sizeof x);
+        memcpy(&v, &value, sizeof v);
+        switch (cmp) {
+        case ORC_LT: return x < v;
+        case ORC_LE: return x <= v;
+        case ORC_GT: return x > v;
+        case ORC_GE: return x >= v;
+        case ORC_EQ: return x == v;
+        default: return x != v;
+        }
+    }
+    switch (cmp) {
+    case ORC_LT: return bits < value;
+    case ORC_LE: return bits <= value;
+    case ORC_GT: return bits > value;
+    case ORC_GE: return bits >= value;
+    case ORC_EQ: return bits == value;
+    default: return bits != value;
+    }
+}
+
+/* Stable select-if with a parameterised predicate; returns the kept count. */
+size_t orc_select_if_cmp(const uint32_t *in, uint32_t *out, size_t n, int dtype, int cmp,
+                         uint32_t value, uint32_t mask)
+{
+    size_t m = 0;
+    for (size_t i = 0; i < n; ++i) {
+        if (keep_cmp(in[i], dtype, cmp, value, mask)) {
+            out[m] = in[i];
+            ++m;
+        }
+    }
+    return m;
+}
+
+/* Stable partition with a parameterised predicate, kept half first. */
+size_t orc_partition_cmp(const uint32_t *in, uint32_t *out, size_t n, int dtype, int cmp,
+                         uint32_t value, uint32_t mask)
+{
+    size_t first = 0;
+    for (size_t i = 0; i < n; ++i) {
+        if (keep_cmp(in[i], dtype, cmp, value, mask)) {
+            out[first] = in[i];
+            ++first;
+        }
+    }
+    size_t second = first;
+    for (size_t i = 0; i < n; ++i) {
+        if (!keep_cmp(in[i], dtype, cmp, value, mask)) {
+            out[second] = in[i];
+            ++second;
+        }
+    }
+    return first;
+}
+
+/*
  * How many positions of an unordered result differ from the stable one.
  * Reported beside the atomic-counter comparator, never used as a pass/fail
  * gate ([Day 33] countOutOfOrder).

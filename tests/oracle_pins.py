@@ -332,6 +332,76 @@ def pin_radix_degenerate(o):
     assert np.array_equal(ko, srt) and np.array_equal(vo, idx)
 
 
+# ------------------------------------------------------------------ parameterised predicates
+
+_NP_CMP = {O.LT: np.less, O.LE: np.less_equal, O.GT: np.greater, O.GE: np.greater_equal,
+           O.EQ: np.equal, O.NE: np.not_equal}
+
+
+def _cmp_inputs(rng, n):
+    xi = rng.integers(-50, 51, size=n).astype(np.int32)
+    xi[::17] = np.iinfo(np.int32).min
+    xi[5::19] = np.iinfo(np.int32).max
+    xu = rng.integers(0, 2 ** 32, size=n, dtype=np.uint64).astype(np.uint32)
+    xu[::13] = 7
+    xf = (rng.standard_normal(n) * 3).astype(np.float32)
+    specials = np.array([0.0, -0.0, np.nan, np.inf, -np.inf, 1e-45, -1e-45, 2.5], np.float32)
+    xf[: 8 * (n // 64)] = np.tile(specials, n // 64)
+    return xi, xu, xf
+
+
+def pin_select_cmp_matches_numpy(o):
+    """x OP v in the dtype's order equals numpy's element-wise comparison
+    (IEEE for float32: NaN compares false except !=), for every operator."""
+    rng = _rng(21)
+    xi, xu, xf = _cmp_inputs(rng, 4096)
+    cases = [(xi, [-50, -3, 0, 7, 2147483647, -2147483648]),
+             (xu, [0, 7, 2 ** 31, 2 ** 32 - 1]),
+             (xf, [0.0, -0.0, 2.5, float("inf"), float("nan"), -1e-45])]
+    for x, values in cases:
+        for v in values:
+            for cmp, f in _NP_CMP.items():
+                want = x[f(x, x.dtype.type(v))]
+                got = o.select_if_cmp(x, cmp, v)
+                assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), (x.dtype, v, cmp)
+
+
+def pin_select_mask_tests_match_numpy(o):
+    """(bits & mask) == value and != value on the raw 32 bits, any dtype."""
+    rng = _rng(22)
+    xi, xu, xf = _cmp_inputs(rng, 4096)
+    for x in (xi, xu, xf):
+        b = x.view(np.uint32)
+        for mask, value in [(1, 0), (1, 1), (0xF0, 0x30), (0x80000000, 0x80000000), (0, 0)]:
+            sel = (b & np.uint32(mask)) == np.uint32(value)
+            assert np.array_equal(o.select_if_cmp(x, O.MASK_EQ, value, mask).view(np.uint32), b[sel])
+            assert np.array_equal(o.select_if_cmp(x, O.MASK_NE, value, mask).view(np.uint32), b[~sel])
+
+
+def pin_fixed_predicates_are_special_cases(o):
+    """ODD = mask 1 != 0, EVEN = mask 1 == 0, NONZERO = != 0 (float: IEEE)."""
+    rng = _rng(23)
+    xi, xu, xf = _cmp_inputs(rng, 2048)
+    for x in (xi, xu):
+        assert np.array_equal(o.select_if_cmp(x, O.MASK_NE, 0, 1), o.select_if(x, O.ODD))
+        assert np.array_equal(o.select_if_cmp(x, O.MASK_EQ, 0, 1), o.select_if(x, O.EVEN))
+        assert np.array_equal(o.select_if_cmp(x, O.NE, 0), o.select_if(x, O.NONZERO))
+    assert np.array_equal(o.select_if_cmp(xf, O.NE, 0.0).view(np.uint32),
+                          o.select_if(xf, O.NONZERO).view(np.uint32))
+
+
+def pin_partition_cmp_invariants(o):
+    """Kept half = numpy-selected elements in order, the rest after, stable."""
+    rng = _rng(24)
+    xi, xu, xf = _cmp_inputs(rng, 3000)
+    for x, v, cmp in [(xi, 3, O.GE), (xu, 2 ** 31, O.LT), (xf, 0.0, O.GT), (xf, 1.0, O.NE)]:
+        sel = _NP_CMP[cmp](x, x.dtype.type(v))
+        got, t = o.partition_cmp(x, cmp, v)
+        assert t == int(sel.sum())
+        assert np.array_equal(got[:t].view(np.uint32), x[sel].view(np.uint32))
+        assert np.array_equal(got[t:].view(np.uint32), x[~sel].view(np.uint32))
+
+
 # ------------------------------------------------------------------ comparator helper
 
 def pin_out_of_order_count(o):

@@ -35,8 +35,8 @@ MUTANTS = [
      "        out[i] = running;\n        running += (double)in[i];",
      "        out[i] = running;\n        running += (double)in[i + (i + 1 < n)];"),
     ("select_writes_wrong_slot",
-     "            out[m] = in[i];\n            ++m;",
-     "            out[m] = in[m];\n            ++m;"),
+     "        if (keep(in[i], dtype, pred)) {\n            out[m] = in[i];\n            ++m;",
+     "        if (keep(in[i], dtype, pred)) {\n            out[m] = in[m];\n            ++m;"),
     ("odd_tests_wrong_bit",
      "    if (pred == ORC_ODD) return (bits & 1u) != 0u;",
      "    if (pred == ORC_ODD) return (bits & 2u) != 0u;"),
@@ -44,8 +44,8 @@ MUTANTS = [
      "        if (dtype == ORC_F32) return bits_to_float(bits) != 0.0f;",
      "        if (dtype == ORC_F32) return bits != 0u;"),
     ("partition_second_half_restarts_at_zero",
-     "    size_t second = first;",
-     "    size_t second = 0;"),
+     "    size_t second = first;\n    for (size_t i = 0; i < n; ++i) {\n        if (!keep(in[i], dtype, pred)) {",
+     "    size_t second = 0;\n    for (size_t i = 0; i < n; ++i) {\n        if (!keep(in[i], dtype, pred)) {"),
     ("partition_second_half_reversed",
      "    size_t second = first;\n    for (size_t i = 0; i < n; ++i) {\n        if (!keep(in[i], dtype, pred)) {",
      "    size_t second = first;\n    for (size_t i = n; i-- > 0;) {\n        if (!keep(in[i], dtype, pred)) {"),
@@ -58,6 +58,15 @@ MUTANTS = [
     ("radix_skips_first_bit",
      "    for (int b = begin_bit; b < end_bit; ++b) {",
      "    for (int b = begin_bit + 1; b < end_bit; ++b) {"),
+    ("cmp_le_as_lt_for_int",
+     "        case ORC_LE: return x <= v;\n        case ORC_GT: return x > v;\n        case ORC_GE: return x >= v;\n        case ORC_EQ: return x == v;\n        default: return x != v;\n        }\n    }\n    switch",
+     "        case ORC_LE: return x < v;\n        case ORC_GT: return x > v;\n        case ORC_GE: return x >= v;\n        case ORC_EQ: return x == v;\n        default: return x != v;\n        }\n    }\n    switch"),
+    ("cmp_unsigned_order_for_int32",
+     "    if (dtype == ORC_I32) {\n        int32_t x, v;",
+     "    if (dtype == 99) {\n        int32_t x, v;"),
+    ("cmp_mask_ignores_mask",
+     "    if (cmp == ORC_MASK_EQ) return (bits & mask) == value;",
+     "    if (cmp == ORC_MASK_EQ) return bits == value;"),
     ("radix_drops_payload_swap",
      "        t = va; va = vb; vb = t;",
      "        (void)0;"),
