@@ -363,6 +363,34 @@ def run_gc(args):
     op_ms = {name: sum(e[name][0].elapsed_time(e[name][1]) for e in evs) / args.steps
              for name in OPS}
 
+    # The widened entry points (not part of the step): inclusive scans and the
+    # parameterised-predicate select / partition on the same 2^28 arrays.
+    pf = gc.predicate(d["f"], ">", 0.75)
+    pi = gc.predicate(d["x"], "<", 0)
+    next_calls = {
+        "inclusive_scan_i32": (lambda: gc.inclusive_scan(d["x"], out=out_a, total=counts[0:1].view(torch.int32), ws=ws, stream=stream), 8.0 * n),
+        "inclusive_scan_f32": (lambda: gc.inclusive_scan(d["f"], out=outf, total=counts[1:2].view(torch.float32), ws=ws, stream=stream), 8.0 * n),
+        "select_pred_f32_gt_0.75": (lambda: gc.select_if_pred(d["f"], pf, out=out_a, count=counts[2:3], ws=ws, stream=stream), None),
+        "partition_pred_i32_lt_0": (lambda: gc.partition_pred(d["x"], pi, out=out_a, count_true=counts[5:6], ws=ws, stream=stream), 8.0 * n + 4),
+    }
+    next_ops = {}
+    for name, (fn, nbytes) in next_calls.items():
+        for _ in range(max(args.warmup, 1)):
+            fn()
+        evn = [(new_ev(), new_ev()) for _ in range(args.steps)]
+        for a_, b_ in evn:
+            a_.record(stream)
+            fn()
+            b_.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = sum(a_.elapsed_time(b_) for a_, b_ in evn) / args.steps
+        if nbytes is None:  # select: read n, write the survivors
+            kept_n = int(counts[2:3].view(torch.int32).item())
+            assert kept_n == int(np.count_nonzero(h["f"] > np.float32(0.75)))
+            nbytes = 4.0 * n + 4.0 * kept_n + 4
+        next_ops[name] = {"ms": round(ms, 4), "gelem_s": round(n / ms / 1e6, 2),
+                          "alg_gbs": round(nbytes / ms / 1e6, 1)}
+
     # End to end: every step copies its inputs in from pinned host memory and
     # every output (and the counts) back, through the C ABI.  Three streams:
     # host-to-device copies, the kernels, device-to-host copies, ordered by
@@ -495,6 +523,7 @@ def run_gc(args):
                          "no flush between steps",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "ops": ops_report,
+        "next_ops": {k: dict(v, frac_of_peak=round(v["alg_gbs"] / peak, 4)) for k, v in next_ops.items()},
         "roofline": {"kernel": "partition_kernel<PredBitClear, payload> (one-bit radix split)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs",

@@ -92,12 +92,44 @@ typedef enum { GC_I32 = 0, GC_U32 = 1, GC_F32 = 2 } gc_dtype;
  */
 typedef enum { GC_PRED_NONZERO = 0, GC_PRED_ODD = 1, GC_PRED_EVEN = 2 } gc_pred;
 
+/*
+ * Parameterised predicates (gc_select_if_pred, gc_partition_pred): "The CUDA
+ * Handbook, ch. 13: Stream compaction" notes that its single-pass compaction
+ * "is easily modified to evaluate more-complicated predicates".
+ *   GC_CMP_LT .. GC_CMP_NE   x OP operand in the dtype's own order: int32
+ *                            signed, uint32 unsigned, float32 IEEE 754 (every
+ *                            comparison with a NaN is false except NE; -0.0
+ *                            equals +0.0).  operand is the value's 32-bit
+ *                            pattern in the dtype.
+ *   GC_CMP_MASK_EQ / _NE     (bits & mask) == operand / != operand on the raw
+ *                            32 bits, any dtype.
+ * The fixed predicates are special cases: NONZERO is NE 0, ODD is MASK_NE
+ * with mask 1 and operand 0, EVEN is MASK_EQ with mask 1 and operand 0.
+ */
+typedef enum {
+    GC_CMP_LT = 0,
+    GC_CMP_LE = 1,
+    GC_CMP_GT = 2,
+    GC_CMP_GE = 3,
+    GC_CMP_EQ = 4,
+    GC_CMP_NE = 5,
+    GC_CMP_MASK_EQ = 6,
+    GC_CMP_MASK_NE = 7
+} gc_cmp;
+
+typedef struct {
+    gc_cmp cmp;
+    uint32_t operand; /* the operand's bits (LT..NE) or the masked value (MASK_*) */
+    uint32_t mask;    /* MASK_* only */
+} gc_predicate;
+
 typedef enum {
     GC_OP_EXCLUSIVE_SCAN = 0,
     GC_OP_SELECT_IF = 1,
     GC_OP_PARTITION = 2,
     GC_OP_SPLIT_RADIX = 3,
-    GC_OP_SELECT_IF_ATOMIC = 4
+    GC_OP_SELECT_IF_ATOMIC = 4,
+    GC_OP_INCLUSIVE_SCAN = 5
 } gc_op;
 
 /* Static, never NULL, "unknown status" for values outside the enum. */
@@ -138,6 +170,17 @@ gc_status gc_exclusive_scan(const void *d_in, void *d_out, void *d_total,
                             size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Inclusive scan: out[i] = in[0] + ... + in[i] (the inclusive scans of
+ * "scan.cu -- Day 31: prefix sum (scan), part 1", whole-array rather than
+ * per block).  Everything else as gc_exclusive_scan, including in-place
+ * operation and d_total.  Workspace: gc_workspace_bytes(GC_OP_INCLUSIVE_SCAN,
+ * ...), the same as the exclusive scan's.
+ */
+gc_status gc_inclusive_scan(const void *d_in, void *d_out, void *d_total,
+                            size_t n, gc_dtype dtype, void *d_ws,
+                            size_t ws_bytes, cudaStream_t stream);
+
+/*
  * Stable select-if.  d_out must have room for n elements (the worst case);
  * elements [0, *d_count) are the survivors in input order, the rest of d_out
  * is untouched.  *d_count is written by the kernel (a uint32 in device
@@ -157,6 +200,20 @@ gc_status gc_select_if(const void *d_in, void *d_out, uint32_t *d_count,
 gc_status gc_partition(const void *d_in, void *d_out, uint32_t *d_count_true,
                        size_t n, gc_dtype dtype, gc_pred pred, void *d_ws,
                        size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * gc_select_if and gc_partition with a parameterised predicate.  `pred` is a
+ * host pointer, read during the call.  GC_ERR_INVALID_VALUE for a NULL pred
+ * or an unknown cmp; otherwise the conventions, workspace
+ * (GC_OP_SELECT_IF / GC_OP_PARTITION) and errors of the fixed-predicate
+ * entry points.
+ */
+gc_status gc_select_if_pred(const void *d_in, void *d_out, uint32_t *d_count,
+                            size_t n, gc_dtype dtype, const gc_predicate *pred,
+                            void *d_ws, size_t ws_bytes, cudaStream_t stream);
+gc_status gc_partition_pred(const void *d_in, void *d_out, uint32_t *d_count_true,
+                            size_t n, gc_dtype dtype, const gc_predicate *pred,
+                            void *d_ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * LSD radix sort by one-bit stable splits over bits [begin_bit, end_bit),

@@ -147,6 +147,7 @@ size_t gc_workspace_bytes(gc_op op, size_t n, gc_dtype dtype)
     const size_t status = status_bytes(max_tiles(n));
     switch (op) {
     case GC_OP_EXCLUSIVE_SCAN:
+    case GC_OP_INCLUSIVE_SCAN:
         if (!valid_dtype(dtype)) return 0;
         return kHeaderBytes + status + (dtype == GC_F32 ? status : 0);
     case GC_OP_SELECT_IF:
@@ -163,7 +164,8 @@ size_t gc_workspace_bytes(gc_op op, size_t n, gc_dtype dtype)
 size_t gc_tile_elements(gc_op op)
 {
     switch (op) {
-    case GC_OP_EXCLUSIVE_SCAN: return scan_tile_elems();
+    case GC_OP_EXCLUSIVE_SCAN:
+    case GC_OP_INCLUSIVE_SCAN: return scan_tile_elems();
     case GC_OP_SELECT_IF: return select_tile_elems();
     case GC_OP_PARTITION: return partition_tile_elems();
     case GC_OP_SPLIT_RADIX: return split_tile_elems();
@@ -179,8 +181,9 @@ gc_status gc_workspace_init(void *d_ws, size_t ws_bytes, cudaStream_t stream)
     return from_cuda(cudaMemsetAsync(d_ws, 0, ws_bytes, stream));
 }
 
-gc_status gc_exclusive_scan(const void *d_in, void *d_out, void *d_total, size_t n,
-                            gc_dtype dtype, void *d_ws, size_t ws_bytes, cudaStream_t stream)
+static gc_status scan_entry(const void *d_in, void *d_out, void *d_total, size_t n,
+                            gc_dtype dtype, void *d_ws, size_t ws_bytes, cudaStream_t stream,
+                            bool inclusive)
 {
     gc_status st = check_common(d_in, d_out, n, d_ws, ws_bytes, GC_OP_EXCLUSIVE_SCAN, dtype);
     if (st != GC_OK) return st;
@@ -194,7 +197,19 @@ gc_status gc_exclusive_scan(const void *d_in, void *d_out, void *d_total, size_t
     if (n == 0)
         return d_total ? from_cuda(cudaMemsetAsync(d_total, 0, 4, stream)) : GC_OK;
     return from_cuda(launch_scan(d_in, d_out, d_total, uint32_t(n), dtype,
-                                 static_cast<uint8_t *>(d_ws), stream, LaunchOpts{}));
+                                 static_cast<uint8_t *>(d_ws), stream, LaunchOpts{}, inclusive));
+}
+
+gc_status gc_exclusive_scan(const void *d_in, void *d_out, void *d_total, size_t n,
+                            gc_dtype dtype, void *d_ws, size_t ws_bytes, cudaStream_t stream)
+{
+    return scan_entry(d_in, d_out, d_total, n, dtype, d_ws, ws_bytes, stream, false);
+}
+
+gc_status gc_inclusive_scan(const void *d_in, void *d_out, void *d_total, size_t n,
+                            gc_dtype dtype, void *d_ws, size_t ws_bytes, cudaStream_t stream)
+{
+    return scan_entry(d_in, d_out, d_total, n, dtype, d_ws, ws_bytes, stream, true);
 }
 
 gc_status gc_select_if(const void *d_in, void *d_out, uint32_t *d_count, size_t n,
@@ -223,6 +238,100 @@ gc_status gc_partition(const void *d_in, void *d_out, uint32_t *d_count_true, si
     if (n == 0) return from_cuda(cudaMemsetAsync(d_count_true, 0, sizeof(uint32_t), stream));
     return from_cuda(launch_partition(d_in, d_out, d_count_true, uint32_t(n), dtype, pred,
                                       static_cast<uint8_t *>(d_ws), stream, LaunchOpts{}));
+}
+
+// Order-preserving unsigned key of a 32-bit pattern in the dtype's order
+// (the device applies the same map to every element).
+static uint32_t order_key(uint32_t bits, gc_dtype dt)
+{
+    if (dt == GC_I32) return bits ^ 0x80000000u;
+    if (dt == GC_F32) return bits ^ ((bits >> 31) ? 0xFFFFFFFFu : 0x80000000u);
+    return bits;
+}
+
+// Keep-interval of a comparison, in keys: [lo, hi], or nothing / everything.
+static void keep_interval(gc_cmp cmp, uint32_t operand, gc_dtype dt, CmpSpec &c)
+{
+    // signed 64-bit: low - 1 below key 0 and high + 1 above 2^32 - 1 stay empty
+    auto set = [&](int64_t lo, int64_t hi, bool inv) {
+        if (lo > hi) {  // empty interval: keep nothing (the complement of everything)
+            c.lo = 0u;
+            c.span = 0xFFFFFFFFu;
+            c.invert = inv ? 0u : 1u;
+        } else {
+            c.lo = uint32_t(lo);
+            c.span = uint32_t(hi - lo);
+            c.invert = inv ? 1u : 0u;
+        }
+    };
+    int64_t kmin = 0, kmax = 0xFFFFFFFFll, low, high;
+    if (dt == GC_F32) {
+        const bool nan = (operand & 0x7F800000u) == 0x7F800000u && (operand & 0x007FFFFFu) != 0u;
+        if (nan) {  // every comparison with NaN is false, except "not equal"
+            set(1, 0, cmp == GC_CMP_NE);
+            return;
+        }
+        kmin = order_key(0xFF800000u, dt);  // -inf
+        kmax = order_key(0x7F800000u, dt);  // +inf
+        const bool zero = (operand & 0x7FFFFFFFu) == 0u;
+        low = zero ? order_key(0x80000000u, dt) : order_key(operand, dt);   // -0.0 first
+        high = zero ? order_key(0x00000000u, dt) : order_key(operand, dt);  // +0.0 last
+    } else {
+        low = high = order_key(operand, dt);
+    }
+    switch (cmp) {
+    case GC_CMP_LT: set(kmin, low - 1, false); break;  // low == kmin gives an empty interval
+    case GC_CMP_LE: set(kmin, high, false); break;
+    case GC_CMP_GT: set(high + 1, kmax, false); break;
+    case GC_CMP_GE: set(low, kmax, false); break;
+    case GC_CMP_EQ: set(low, high, false); break;
+    default: set(low, high, true); break;  // GC_CMP_NE
+    }
+}
+
+static bool cmp_spec(const gc_predicate *pred, gc_dtype dt, CmpSpec &c)
+{
+    if (pred == nullptr) return false;
+    const int cmp = int(pred->cmp);
+    if (cmp < GC_CMP_LT || cmp > GC_CMP_MASK_NE) return false;
+    c = CmpSpec{};
+    if (cmp >= GC_CMP_MASK_EQ) {
+        c.is_mask = 1u;
+        c.mask = pred->mask;
+        c.value = pred->operand;
+        c.invert = cmp == GC_CMP_MASK_NE ? 1u : 0u;
+    } else {
+        keep_interval(gc_cmp(cmp), pred->operand, dt, c);
+    }
+    return true;
+}
+
+gc_status gc_select_if_pred(const void *d_in, void *d_out, uint32_t *d_count, size_t n,
+                            gc_dtype dtype, const gc_predicate *pred, void *d_ws, size_t ws_bytes,
+                            cudaStream_t stream)
+{
+    CmpSpec c;
+    if (!cmp_spec(pred, dtype, c)) return GC_ERR_INVALID_VALUE;
+    gc_status st = check_select_like(d_in, d_out, d_count, n, dtype, GC_PRED_NONZERO, d_ws,
+                                     ws_bytes, GC_OP_SELECT_IF);
+    if (st != GC_OK) return st;
+    if (n == 0) return from_cuda(cudaMemsetAsync(d_count, 0, sizeof(uint32_t), stream));
+    return from_cuda(launch_select_cmp(d_in, d_out, d_count, uint32_t(n), dtype, c,
+                                       static_cast<uint8_t *>(d_ws), stream, LaunchOpts{}));
+}
+
+gc_status gc_partition_pred(const void *d_in, void *d_out, uint32_t *d_count_true, size_t n,
+                            gc_dtype dtype, const gc_predicate *pred, void *d_ws, size_t ws_bytes,
+                            cudaStream_t stream)
+{
+    CmpSpec c;
+    if (!cmp_spec(pred, dtype, c)) return GC_ERR_INVALID_VALUE;
+    gc_status st = check_select_like(d_in, d_out, d_count_true, n, dtype, GC_PRED_NONZERO, d_ws,
+                                     ws_bytes, GC_OP_PARTITION);
+    if (st != GC_OK) return st;
+    if (n == 0) return from_cuda(cudaMemsetAsync(d_count_true, 0, sizeof(uint32_t), stream));
+    return from_cuda(launch_partition_cmp(d_in, d_out, d_count_true, uint32_t(n), dtype, c,
+                                          static_cast<uint8_t *>(d_ws), stream, LaunchOpts{}));
 }
 
 gc_status gc_split_radix(const uint32_t *d_keys_in, const uint32_t *d_vals_in,

@@ -267,6 +267,37 @@ struct PredOdd {
 struct PredEven {
     __device__ __forceinline__ bool operator()(uint32_t x) const { return (x & 1u) == 0u; }
 };
+// Parameterised predicate ("The CUDA Handbook, ch. 13": the compaction "is
+// easily modified to evaluate more-complicated predicates"): a comparison
+// with an operand in the dtype's own order (DT 0: int32 signed, 1: uint32
+// unsigned, 2: float32 IEEE 754) or a test of the raw bits under a mask.
+// Every element is mapped to an order-preserving unsigned key (int32: flip
+// the sign bit; float32: flip the sign bit of positives and every bit of
+// negatives, so keys ascend with the value and NaNs fall outside
+// [key(-inf), key(+inf)]); each comparison then keeps one key interval
+// [lo, lo + span] or, with invert, its complement.  The host turns the
+// operator and operand into (lo, span, invert), treating -0.0 and +0.0 as
+// equal and NaN operands as IEEE does, so each element costs a subtract, an
+// unsigned compare and an xor.  A mask test keeps (x & mask) == value,
+// inverted for "not equal".
+template <int DT>
+struct PredCmp {
+    uint32_t lo;
+    uint32_t span;
+    uint32_t invert;
+    uint32_t is_mask;
+    uint32_t mask;
+    uint32_t value;
+    __device__ __forceinline__ bool operator()(uint32_t x) const
+    {
+        if (is_mask) return ((x & mask) == value) != (invert != 0u);
+        uint32_t k = x;
+        if (DT == 0) k = x ^ 0x80000000u;
+        if (DT == 2) k = x ^ (uint32_t(int32_t(x) >> 31) | 0x80000000u);
+        return ((k - lo) <= span) != (invert != 0u);
+    }
+};
+
 // Radix split: "bit b is clear" goes first.
 struct PredBitClear {
     uint32_t bit;

@@ -134,7 +134,18 @@ cudaError_t clear_accumulators(uint8_t *ws, cudaStream_t s);
 
 // Launchers.  All arguments were validated by api.cu; n >= 1.
 cudaError_t launch_scan(const void *in, void *out, void *total, uint32_t n, gc_dtype dt,
-                        uint8_t *ws, cudaStream_t s, const LaunchOpts &o);
+                        uint8_t *ws, cudaStream_t s, const LaunchOpts &o, bool inclusive = false);
+
+// A parameterised predicate as the kernels take it (see gcd::PredCmp): keep
+// keys in [lo, lo + span] (xor invert), or (x & mask) == value (xor invert).
+struct CmpSpec {
+    uint32_t lo, span, invert, is_mask, mask, value;
+};
+cudaError_t launch_select_cmp(const void *in, void *out, uint32_t *count, uint32_t n, gc_dtype dt,
+                              const CmpSpec &c, uint8_t *ws, cudaStream_t s, const LaunchOpts &o);
+cudaError_t launch_partition_cmp(const void *in, void *out, uint32_t *count_true, uint32_t n,
+                                 gc_dtype dt, const CmpSpec &c, uint8_t *ws, cudaStream_t s,
+                                 const LaunchOpts &o);
 cudaError_t launch_select(const void *in, void *out, uint32_t *count, uint32_t n, gc_dtype dt,
                           gc_pred p, uint8_t *ws, cudaStream_t s, const LaunchOpts &o);
 cudaError_t launch_select_atomic(const void *in, void *out, uint32_t *count, uint32_t n,

@@ -223,7 +223,7 @@ __device__ __forceinline__ void tile_vectors(const uint32_t *sbuf, const uint32_
 }
 
 // Exclusive scan, uint32 (int32 bits) or float32.
-template <int THREADS, int ROWS, bool F32, bool OUT_VEC>
+template <int THREADS, int ROWS, bool F32, bool OUT_VEC, bool INCL = false>
 struct ScanOp {
     using TT = Tile<THREADS, ROWS>;
     static constexpr uint32_t kTileElems = TT::kElems;
@@ -303,8 +303,9 @@ struct ScanOp {
             uint32_t o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
+                if (INCL) v += x[r][q];   // inclusive: the element itself counts
                 o[q] = v;
-                v += x[r][q];
+                if (!INCL) v += x[r][q];
             }
             store4<OUT_VEC && !FULL>(out, base + r * TT::kRowElems + 4 * tid, n, o, FULL && OUT_VEC);
         }
@@ -348,8 +349,9 @@ struct ScanOp {
             uint32_t o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
+                if (INCL) local += __uint_as_float(x[r][q]);
                 o[q] = __float_as_uint(hi + (lo + local));
-                local += __uint_as_float(x[r][q]);
+                if (!INCL) local += __uint_as_float(x[r][q]);
             }
             store4<OUT_VEC && !FULL>(out, base + r * TT::kRowElems + 4 * tid, n, o, FULL && OUT_VEC);
         }

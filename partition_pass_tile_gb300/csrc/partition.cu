@@ -366,6 +366,22 @@ cudaError_t launch_partition(const void *in, void *out, uint32_t *count_true, ui
     }
 }
 
+cudaError_t launch_partition_cmp(const void *in, void *out, uint32_t *count_true, uint32_t n,
+                                 gc_dtype dt, const CmpSpec &c, uint8_t *ws, cudaStream_t s,
+                                 const LaunchOpts &o)
+{
+    auto *i = static_cast<const uint32_t *>(in);
+    auto *u = static_cast<uint32_t *>(out);
+    if (dt == GC_I32)
+        return dispatch_partition(i, u, count_true, n,
+                                  gcd::PredCmp<0>{c.lo, c.span, c.invert, c.is_mask, c.mask, c.value}, ws, s, o);
+    if (dt == GC_U32)
+        return dispatch_partition(i, u, count_true, n,
+                                  gcd::PredCmp<1>{c.lo, c.span, c.invert, c.is_mask, c.mask, c.value}, ws, s, o);
+    return dispatch_partition(i, u, count_true, n,
+                              gcd::PredCmp<2>{c.lo, c.span, c.invert, c.is_mask, c.mask, c.value}, ws, s, o);
+}
+
 cudaError_t launch_split_radix(const uint32_t *keys_in, const uint32_t *vals_in,
                                uint32_t *keys_out, uint32_t *vals_out, uint32_t n, int begin_bit,
                                int end_bit, uint8_t *ws, cudaStream_t s, const LaunchOpts &o)

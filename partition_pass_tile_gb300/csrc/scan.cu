@@ -28,7 +28,7 @@ namespace {
 
 using namespace gcd;
 
-template <int THREADS, int ROWS, bool VEC, bool LB>
+template <int THREADS, int ROWS, bool VEC, bool LB, bool INCL>
 __global__ void __launch_bounds__(THREADS)
 scan_u32_kernel(const uint32_t *in, uint32_t *out, uint32_t *total, uint32_t n,
                 uint32_t num_tiles, uint8_t *ws, uint64_t timeout_ns)
@@ -72,8 +72,9 @@ scan_u32_kernel(const uint32_t *in, uint32_t *out, uint32_t *total, uint32_t n,
         uint32_t o[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
+            if (INCL) v += x[r][k];
             o[k] = v;
-            v += x[r][k];
+            if (!INCL) v += x[r][k];
         }
         store4<VEC>(out, base + r * TT::kRowElems + 4 * tid, n, o);
     }
@@ -84,7 +85,7 @@ scan_u32_kernel(const uint32_t *in, uint32_t *out, uint32_t *total, uint32_t n,
 // hi + lo (hi = the double rounded to float, lo = the remainder rounded to
 // float), and each output is hi + (lo + local).  The carry between tiles
 // therefore never rounds to float32 before the last add of each element.
-template <int THREADS, int ROWS, bool VEC, bool LB>
+template <int THREADS, int ROWS, bool VEC, bool LB, bool INCL>
 __global__ void __launch_bounds__(THREADS)
 scan_f32_kernel(const uint32_t *in_bits, uint32_t *out_bits, uint32_t *total_bits, uint32_t n,
                 uint32_t num_tiles, uint8_t *ws, double *prefix64, uint64_t timeout_ns)
@@ -134,8 +135,9 @@ scan_f32_kernel(const uint32_t *in_bits, uint32_t *out_bits, uint32_t *total_bit
         uint32_t o[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
+            if (INCL) local += __uint_as_float(raw[r][k]);
             o[k] = __float_as_uint(hi + (lo + local));
-            local += __uint_as_float(raw[r][k]);
+            if (!INCL) local += __uint_as_float(raw[r][k]);
         }
         store4<VEC>(out_bits, base + r * TT::kRowElems + 4 * tid, n, o);
     }
@@ -149,19 +151,18 @@ uint32_t scan_tile_elems() { return tile_elems(kScanPipeThreads, kScanPipeRows);
 
 namespace {
 
-template <bool F32, bool OUT_VEC>
+template <bool F32, bool OUT_VEC, bool INCL>
 cudaError_t launch_scan_pipe(const uint32_t *in, uint32_t *out, uint32_t *total, uint32_t n,
                              uint8_t *ws, cudaStream_t s, const LaunchOpts &o)
 {
-    using Op = gcd::ScanOp<kScanPipeThreads, kScanPipeRows, F32, OUT_VEC>;
+    using Op = gcd::ScanOp<kScanPipeThreads, kScanPipeRows, F32, OUT_VEC, INCL>;
     Op op{{in}, out, total};
     return gcd::launch_pipeline<kScanPipeThreads, kScanPipeStages>(op, n, ws, s, o.timeout_ns);
 }
 
-}  // namespace
-
-cudaError_t launch_scan(const void *in, void *out, void *total, uint32_t n, gc_dtype dt,
-                        uint8_t *ws, cudaStream_t s, const LaunchOpts &o)
+template <bool INCL>
+cudaError_t launch_scan_impl(const void *in, void *out, void *total, uint32_t n, gc_dtype dt,
+                             uint8_t *ws, cudaStream_t s, const LaunchOpts &o)
 {
     auto *i = static_cast<const uint32_t *>(in);
     auto *u = static_cast<uint32_t *>(out);
@@ -170,11 +171,11 @@ cudaError_t launch_scan(const void *in, void *out, void *total, uint32_t n, gc_d
     if (aligned16(in) && !o.skip_first_tile) {
         const bool ov = aligned16(out);
         if (dt == GC_F32)
-            e = ov ? launch_scan_pipe<true, true>(i, u, t, n, ws, s, o)
-                   : launch_scan_pipe<true, false>(i, u, t, n, ws, s, o);
+            e = ov ? launch_scan_pipe<true, true, INCL>(i, u, t, n, ws, s, o)
+                   : launch_scan_pipe<true, false, INCL>(i, u, t, n, ws, s, o);
         else
-            e = ov ? launch_scan_pipe<false, true>(i, u, t, n, ws, s, o)
-                   : launch_scan_pipe<false, false>(i, u, t, n, ws, s, o);
+            e = ov ? launch_scan_pipe<false, true, INCL>(i, u, t, n, ws, s, o)
+                   : launch_scan_pipe<false, false, INCL>(i, u, t, n, ws, s, o);
         if (e == cudaSuccess) return e;
         // The device cannot hold the whole cooperative grid right now (another
         // context holds SMs): fall through to the kernel that needs no
@@ -193,20 +194,29 @@ cudaError_t launch_scan(const void *in, void *out, void *total, uint32_t n, gc_d
     if (dt == GC_F32) {
         double *prefix64 = reinterpret_cast<double *>(ws + kHeaderBytes + status_bytes(tiles));
         if (vec)
-            scan_f32_kernel<kScanThreads, kScanRows, true, kCtaLookback>
+            scan_f32_kernel<kScanThreads, kScanRows, true, kCtaLookback, INCL>
                 <<<grid, kScanThreads, 0, s>>>(i, u, t, n, tiles, ws, prefix64, o.timeout_ns);
         else
-            scan_f32_kernel<kScanThreads, kScanRows, false, kCtaLookback>
+            scan_f32_kernel<kScanThreads, kScanRows, false, kCtaLookback, INCL>
                 <<<grid, kScanThreads, 0, s>>>(i, u, t, n, tiles, ws, prefix64, o.timeout_ns);
     } else {
         if (vec)
-            scan_u32_kernel<kScanThreads, kScanRows, true, kCtaLookback>
+            scan_u32_kernel<kScanThreads, kScanRows, true, kCtaLookback, INCL>
                 <<<grid, kScanThreads, 0, s>>>(i, u, t, n, tiles, ws, o.timeout_ns);
         else
-            scan_u32_kernel<kScanThreads, kScanRows, false, kCtaLookback>
+            scan_u32_kernel<kScanThreads, kScanRows, false, kCtaLookback, INCL>
                 <<<grid, kScanThreads, 0, s>>>(i, u, t, n, tiles, ws, o.timeout_ns);
     }
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_scan(const void *in, void *out, void *total, uint32_t n, gc_dtype dt,
+                        uint8_t *ws, cudaStream_t s, const LaunchOpts &o, bool inclusive)
+{
+    return inclusive ? launch_scan_impl<true>(in, out, total, n, dt, ws, s, o)
+                     : launch_scan_impl<false>(in, out, total, n, dt, ws, s, o);
 }
 
 }  // namespace gch

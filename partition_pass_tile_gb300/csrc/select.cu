@@ -197,6 +197,18 @@ cudaError_t launch_select(const void *in, void *out, uint32_t *count, uint32_t n
     }
 }
 
+cudaError_t launch_select_cmp(const void *in, void *out, uint32_t *count, uint32_t n, gc_dtype dt,
+                              const CmpSpec &c, uint8_t *ws, cudaStream_t s, const LaunchOpts &o)
+{
+    auto *i = static_cast<const uint32_t *>(in);
+    auto *u = static_cast<uint32_t *>(out);
+    if (dt == GC_I32)
+        return dispatch_select(i, u, count, n, gcd::PredCmp<0>{c.lo, c.span, c.invert, c.is_mask, c.mask, c.value}, ws, s, o);
+    if (dt == GC_U32)
+        return dispatch_select(i, u, count, n, gcd::PredCmp<1>{c.lo, c.span, c.invert, c.is_mask, c.mask, c.value}, ws, s, o);
+    return dispatch_select(i, u, count, n, gcd::PredCmp<2>{c.lo, c.span, c.invert, c.is_mask, c.mask, c.value}, ws, s, o);
+}
+
 cudaError_t launch_select_atomic(const void *in, void *out, uint32_t *count, uint32_t n,
                                  gc_dtype dt, gc_pred p, cudaStream_t s)
 {

@@ -24,6 +24,15 @@ LIB_PATH = Path(__file__).resolve().parent / "libgc.so"
 I32, U32, F32 = 0, 1, 2
 NONZERO, ODD, EVEN = 0, 1, 2
 OP_EXCLUSIVE_SCAN, OP_SELECT_IF, OP_PARTITION, OP_SPLIT_RADIX, OP_SELECT_IF_ATOMIC = range(5)
+OP_INCLUSIVE_SCAN = 5
+LT, LE, GT, GE, EQ, NE, MASK_EQ, MASK_NE = range(8)
+CMP_NAMES = {"<": LT, "<=": LE, ">": GT, ">=": GE, "==": EQ, "!=": NE,
+             "mask==": MASK_EQ, "mask!=": MASK_NE}
+
+
+class Predicate(ctypes.Structure):
+    """gc_predicate: x OP operand in the dtype's order, or (bits & mask) OP operand."""
+    _fields_ = [("cmp", ctypes.c_int), ("operand", ctypes.c_uint32), ("mask", ctypes.c_uint32)]
 STATUS = {0: "GC_OK", 1: "GC_ERR_INVALID_VALUE", 2: "GC_ERR_UNSUPPORTED",
           3: "GC_ERR_WORKSPACE_TOO_SMALL", 4: "GC_ERR_MISALIGNED", 5: "GC_ERR_CUDA",
           6: "GC_ERR_TIMEOUT", 7: "GC_ERR_DEVICE_CHECK"}
@@ -63,6 +72,9 @@ def load(path: str | Path | None = None) -> ctypes.CDLL:
         "gc_select_if_atomic": ([V, V, V, Z, I, I, V, Z, V], S),
         "gc_query_device_status": ([V, V], S),
         "gc_testing_select_if_skip_tile0": ([V, V, V, Z, I, I, V, Z, U64, V], S),
+        "gc_inclusive_scan": ([V, V, V, Z, I, V, Z, V], S),
+        "gc_select_if_pred": ([V, V, V, Z, I, ctypes.POINTER(Predicate), V, Z, V], S),
+        "gc_partition_pred": ([V, V, V, Z, I, ctypes.POINTER(Predicate), V, Z, V], S),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -140,6 +152,67 @@ def exclusive_scan(x: torch.Tensor, out: torch.Tensor | None = None,
     _check(load().gc_exclusive_scan(_ptr(x), _ptr(out), _ptr(total), n, dt, _ptr(ws),
                                     ws.numel(), _stream(stream)), "gc_exclusive_scan")
     return out, total
+
+
+def inclusive_scan(x: torch.Tensor, out: torch.Tensor | None = None,
+                   total: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                   stream=None, with_total: bool = True):
+    """-> (out, total) with out[i] = x[0] + ... + x[i]."""
+    n = x.numel()
+    dt = dtype_code(x)
+    if out is None:
+        out = torch.empty_like(x)
+    if total is None and with_total:
+        total = torch.empty(1, dtype=x.dtype, device=x.device)
+    ws = _ws(ws, OP_INCLUSIVE_SCAN, n, dt, x.device)
+    _check(load().gc_inclusive_scan(_ptr(x), _ptr(out), _ptr(total), n, dt, _ptr(ws),
+                                    ws.numel(), _stream(stream)), "gc_inclusive_scan")
+    return out, total
+
+
+def predicate(x: torch.Tensor, cmp, operand=0, mask: int = 0) -> Predicate:
+    """A gc_predicate for tensor x: cmp in "<", "<=", ">", ">=", "==", "!=" (operand
+    a number of x's dtype) or "mask==", "mask!=" (operand, mask: raw 32-bit patterns)."""
+    c = CMP_NAMES[cmp] if isinstance(cmp, str) else int(cmp)
+    if c >= MASK_EQ:
+        bits = int(operand) & 0xFFFFFFFF
+    else:
+        np_dtype = {torch.int32: "<i4", torch.uint32: "<u4", torch.float32: "<f4"}[x.dtype]
+        import numpy as np
+        bits = int(np.array([operand], dtype=np_dtype).view(np.uint32)[0])
+    return Predicate(c, bits, int(mask) & 0xFFFFFFFF)
+
+
+def select_if_pred(x: torch.Tensor, pred: Predicate, out: torch.Tensor | None = None,
+                   count: torch.Tensor | None = None, ws: torch.Tensor | None = None, stream=None):
+    """Stable select-if with a parameterised predicate -> (out, count)."""
+    n = x.numel()
+    dt = dtype_code(x)
+    if out is None:
+        out = torch.empty_like(x)
+    if count is None:
+        count = torch.empty(1, dtype=torch.uint32, device=x.device)
+    ws = _ws(ws, OP_SELECT_IF, n, dt, x.device)
+    _check(load().gc_select_if_pred(_ptr(x), _ptr(out), _ptr(count), n, dt, ctypes.byref(pred),
+                                    _ptr(ws), ws.numel(), _stream(stream)), "gc_select_if_pred")
+    return out, count
+
+
+def partition_pred(x: torch.Tensor, pred: Predicate, out: torch.Tensor | None = None,
+                   count_true: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                   stream=None):
+    """Stable partition with a parameterised predicate -> (out, count_true)."""
+    n = x.numel()
+    dt = dtype_code(x)
+    if out is None:
+        out = torch.empty_like(x)
+    if count_true is None:
+        count_true = torch.empty(1, dtype=torch.uint32, device=x.device)
+    ws = _ws(ws, OP_PARTITION, n, dt, x.device)
+    _check(load().gc_partition_pred(_ptr(x), _ptr(out), _ptr(count_true), n, dt,
+                                    ctypes.byref(pred), _ptr(ws), ws.numel(), _stream(stream)),
+           "gc_partition_pred")
+    return out, count_true
 
 
 def select_if(x: torch.Tensor, pred, out: torch.Tensor | None = None,

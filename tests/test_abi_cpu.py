@@ -37,7 +37,8 @@ def test_header_declares_the_entry_points():
     for want in ["gc_exclusive_scan", "gc_select_if", "gc_partition", "gc_split_radix",
                  "gc_select_if_atomic", "gc_workspace_bytes", "gc_query_device_status",
                  "gc_status_string", "gc_workspace_init", "gc_tile_elements",
-                 "gc_testing_select_if_skip_tile0"]:
+                 "gc_testing_select_if_skip_tile0", "gc_inclusive_scan", "gc_select_if_pred",
+                 "gc_partition_pred", "gc_select_if_noalloc"]:
         assert want in names
 
 
@@ -118,6 +119,37 @@ def test_scan_validation(lib):
     assert f(IN, OUT, None, 1000, 3, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
     assert f(IN, OUT, None, 1000, gc.F32, WS, 530, None) == E["GC_ERR_WORKSPACE_TOO_SMALL"]
     assert f(None, OUT, None, 1000, gc.I32, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+
+
+def test_pred_validation(lib):
+    E = {v: k for k, v in gc.STATUS.items()}
+    good = gc.Predicate(gc.LT, 5, 0)
+    for fn in (lib.gc_select_if_pred, lib.gc_partition_pred):
+        assert fn(IN, OUT, CNT, 1000, gc.I32, None, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+        bad = gc.Predicate(8, 0, 0)
+        assert fn(IN, OUT, CNT, 1000, gc.I32, bad, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+        bad = gc.Predicate(-1, 0, 0)
+        assert fn(IN, OUT, CNT, 1000, gc.I32, bad, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+        # float32 accepts every comparison (unlike ODD/EVEN); the other checks still apply
+        assert fn(IN + 2, OUT, CNT, 1000, gc.F32, good, WS, BIG, None) == E["GC_ERR_MISALIGNED"]
+        assert fn(IN, OUT, CNT, 1000, gc.F32, good, WS, 100, None) == E["GC_ERR_WORKSPACE_TOO_SMALL"]
+        assert fn(IN, IN + 40, CNT, 1000, gc.I32, good, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+    f = lib.gc_inclusive_scan
+    assert f(IN, IN + 8, None, 1000, gc.I32, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+    assert f(IN, OUT, None, 2 ** 31, gc.I32, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+    assert lib.gc_workspace_bytes(gc.OP_INCLUSIVE_SCAN, 1 << 20, gc.F32) == \
+        lib.gc_workspace_bytes(gc.OP_EXCLUSIVE_SCAN, 1 << 20, gc.F32)
+
+
+def test_predicate_helper_bits():
+    import torch
+    x = torch.zeros(1, dtype=torch.float32)
+    p = gc.predicate(x, "<", 2.5)
+    assert p.cmp == gc.LT and p.operand == 0x40200000
+    p = gc.predicate(torch.zeros(1, dtype=torch.int32), ">=", -1)
+    assert p.operand == 0xFFFFFFFF
+    p = gc.predicate(x, "mask!=", 0, 1)
+    assert (p.cmp, p.operand, p.mask) == (gc.MASK_NE, 0, 1)
 
 
 def test_radix_validation(lib):
