@@ -23,6 +23,9 @@ Parity status of each function (what pins it, in ``tests/test_oracle_pins.py``):
   invariants, the i - rank[i] identity.
 * split_radix: numpy's stable argsort (a library routine) on keys, payload
   permutation, single-bit case against partition.
+* radix_sort (typed keys): numpy's stable argsort on int32 / float32 keys
+  without NaN or -0.0, a hand-written totalOrder sequence of float special
+  values, and split_radix for uint32.
 * select_if_cmp / partition_cmp: numpy's element-wise comparisons and
   masked-bit tests (library routines, IEEE semantics for float32) on inputs
   with every float special value; the fixed predicates as special cases.
@@ -93,6 +96,8 @@ def load_library(path: str | os.PathLike | None = None) -> ctypes.CDLL:
     lib.orc_select_if_cmp.restype = Z
     lib.orc_partition_cmp.argtypes = [P, P, Z, I, I, U, U]
     lib.orc_partition_cmp.restype = Z
+    lib.orc_radix_sort.argtypes = [P, P, P, P, Z, I]
+    lib.orc_radix_sort.restype = I
     lib.orc_count_out_of_order.argtypes = [P, P, Z]
     lib.orc_count_out_of_order.restype = Z
     return lib
@@ -211,6 +216,22 @@ class Oracle:
                                           keys.shape[0], begin_bit, end_bit)
         if rc != 0:
             raise ValueError("orc_split_radix rejected its arguments")
+        return ko, vo
+
+    def radix_sort(self, keys: np.ndarray, vals: np.ndarray | None = None):
+        """Stable ascending sort in keys' dtype order (float32: IEEE totalOrder)."""
+        keys = _c(keys)
+        dt = _dtype_code(keys)
+        ko = np.empty_like(keys)
+        if vals is not None:
+            vals = _c(vals.astype(np.uint32, copy=False))
+            vo = np.empty_like(vals)
+            rc = self.lib.orc_radix_sort(_ptr(keys), _ptr(vals), _ptr(ko), _ptr(vo), keys.shape[0], dt)
+        else:
+            vo = None
+            rc = self.lib.orc_radix_sort(_ptr(keys), None, _ptr(ko), None, keys.shape[0], dt)
+        if rc != 0:
+            raise ValueError("orc_radix_sort rejected its arguments")
         return ko, vo
 
     def count_out_of_order(self, got: np.ndarray, want: np.ndarray) -> int:

@@ -402,6 +402,44 @@ def pin_partition_cmp_invariants(o):
         assert np.array_equal(got[t:].view(np.uint32), x[~sel].view(np.uint32))
 
 
+# ------------------------------------------------------------------ typed radix sort
+
+def pin_radix_sort_int32_float32_match_argsort(o):
+    """int32 and float32 keys (no NaN, no -0.0) sort as numpy's stable argsort;
+    uint32 keys as the 32-bit one-bit-split sort."""
+    rng = _rng(31)
+    ki = rng.integers(-2 ** 31, 2 ** 31, size=50_001, dtype=np.int64).astype(np.int32)
+    ki[::9] = ki[4]
+    kf = (rng.standard_normal(50_001) * 1e3).astype(np.float32)
+    kf[::7] = kf[3]
+    kf[5::11] = np.float32(np.inf)
+    kf[6::13] = np.float32(-np.inf)
+    kf[kf == 0] = 1.0  # keep -0.0 out: numpy orders it equal to +0.0
+    vals = np.arange(50_001, dtype=np.uint32)
+    for k in (ki, kf):
+        perm = np.argsort(k, kind="stable")
+        ko, vo = o.radix_sort(k, vals)
+        assert np.array_equal(ko.view(np.uint32), k[perm].view(np.uint32))
+        assert np.array_equal(vo, perm.astype(np.uint32))
+    ku = synth.uniform_u32(20_001, 6)
+    ko, vo = o.radix_sort(ku, vals[:20_001])
+    wk, wv = o.split_radix(ku, vals[:20_001])
+    assert np.array_equal(ko, wk) and np.array_equal(vo, wv)
+
+
+def pin_radix_sort_float_total_order(o):
+    """IEEE 754 totalOrder: -NaN < -inf < -1 < -denormal < -0 < +0 < +denormal
+    < 1 < +inf < +NaN, ties in input order."""
+    order = [0xFFC00000, 0xFF800000, 0xBF800000, 0x80000001, 0x80000000, 0x00000000,
+             0x00000001, 0x3F800000, 0x7F800000, 0x7FC00000]
+    keys = np.array([order[i] for i in (7, 0, 5, 9, 4, 2, 8, 1, 6, 3, 5, 4)],
+                    dtype=np.uint32).view(np.float32)
+    ko, vo = o.radix_sort(keys, np.arange(12, dtype=np.uint32))
+    want = [order[i] for i in (0, 1, 2, 3, 4, 4, 5, 5, 6, 7, 8, 9)]
+    assert ko.view(np.uint32).tolist() == want
+    assert vo.tolist() == [1, 7, 5, 9, 4, 11, 2, 10, 8, 0, 6, 3]
+
+
 # ------------------------------------------------------------------ comparator helper
 
 def pin_out_of_order_count(o):

@@ -67,6 +67,12 @@ MUTANTS = [
     ("cmp_mask_ignores_mask",
      "    if (cmp == ORC_MASK_EQ) return (bits & mask) == value;",
      "    if (cmp == ORC_MASK_EQ) return bits == value;"),
+    ("float_key_positive_not_flipped",
+     "    if (dtype == ORC_F32) return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);",
+     "    if (dtype == ORC_F32) return (bits & 0x80000000u) ? ~bits : bits;"),
+    ("int32_key_unsigned_order",
+     "    if (dtype == ORC_I32) return bits ^ 0x80000000u;\n    if (dtype == ORC_F32) return (bits & 0x80000000u) ? ~bits",
+     "    if (dtype == ORC_I32) return bits;\n    if (dtype == ORC_F32) return (bits & 0x80000000u) ? ~bits"),
     ("radix_drops_payload_swap",
      "        t = va; va = vb; vb = t;",
      "        (void)0;"),
