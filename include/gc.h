@@ -26,6 +26,12 @@
  *                        "CIS 565 Project 2: Stream Compaction" (radix sort
  *                        built on scan); each split is gc_partition with the
  *                        predicate "bit b is 0".
+ *   gc_radix_sort        full-width stable ascending sort of int32, uint32 or
+ *                        float32 keys (IEEE 754 totalOrder), the same one-bit
+ *                        splits over an order-preserving key.  The radix
+ *                        passage sorts unsigned keys only; the key map is
+ *                        the standard sign-flip reading of "sort by the
+ *                        value" for the other two dtypes.
  *   gc_select_if_atomic  the comparison path: the same survivors and count,
  *                        placed by an atomic counter, in no defined order.
  *                        "compaction.cu -- Day 33" (compactAtomic).
@@ -129,7 +135,8 @@ typedef enum {
     GC_OP_PARTITION = 2,
     GC_OP_SPLIT_RADIX = 3,
     GC_OP_SELECT_IF_ATOMIC = 4,
-    GC_OP_INCLUSIVE_SCAN = 5
+    GC_OP_INCLUSIVE_SCAN = 5,
+    GC_OP_RADIX_SORT = 6
 } gc_op;
 
 /* Static, never NULL, "unknown status" for values outside the enum. */
@@ -140,7 +147,8 @@ const char *gc_version(void);
 
 /*
  * Workspace bytes op needs for n elements of dtype (dtype is ignored for
- * GC_OP_SPLIT_RADIX, whose keys and payloads are uint32).  Returns 0 for an
+ * GC_OP_SPLIT_RADIX, whose keys and payloads are uint32; GC_OP_RADIX_SORT
+ * needs the same bytes for every dtype).  Returns 0 for an
  * unknown op or dtype or n > GC_MAX_ELEMENTS.  A workspace sized for the
  * largest (op, n) it will serve can be reused by every smaller call.
  */
@@ -231,6 +239,24 @@ gc_status gc_split_radix(const uint32_t *d_keys_in, const uint32_t *d_vals_in,
                          uint32_t *d_keys_out, uint32_t *d_vals_out, size_t n,
                          int begin_bit, int end_bit, void *d_ws,
                          size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Stable ascending radix sort of n keys of dtype, payloads carried: int32 in
+ * signed order, uint32 in unsigned order, float32 in IEEE 754 totalOrder
+ * (-NaN < -inf < negatives < -0 < +0 < positives < +inf < +NaN; NaNs by
+ * payload bits, as patterns).  Equal keys keep their input order.  Bit b of
+ * the order-preserving key k(x) = x ^ (signfill(x) & neg) ^ flip (int32: neg
+ * 0, flip 2^31; float32: neg 2^31 - 1, flip 2^31; uint32: both 0) drives
+ * split b, b = 0..31; the keys are moved as they are, never rewritten, so
+ * d_keys_out holds the input's own bit patterns.  Same array rules, aliasing
+ * and workspace layout as gc_split_radix (workspace:
+ * gc_workspace_bytes(GC_OP_RADIX_SORT, n, dtype)).  Keys are d_keys_in /
+ * d_keys_out as void * to any of the three dtypes, 4-byte aligned.
+ */
+gc_status gc_radix_sort(const void *d_keys_in, const uint32_t *d_vals_in,
+                        void *d_keys_out, uint32_t *d_vals_out, size_t n,
+                        gc_dtype dtype, void *d_ws, size_t ws_bytes,
+                        cudaStream_t stream);
 
 /*
  * The atomic-counter comparison path: the same survivors and the same

@@ -106,6 +106,30 @@ gc_status check_select_like(const void *in, const void *out, const uint32_t *cou
     return GC_OK;
 }
 
+// Pairing, alignment and aliasing rules of the radix entry points: keys and
+// payloads come both or keys alone, each input may equal its output, and no
+// other pair of the four arrays (or the workspace) overlaps.
+gc_status check_radix_arrays(const void *keys_in, const uint32_t *vals_in, const void *keys_out,
+                             const uint32_t *vals_out, size_t n, void *ws, size_t ws_bytes)
+{
+    if ((vals_in == nullptr) != (vals_out == nullptr)) return GC_ERR_INVALID_VALUE;
+    if (n == 0) return GC_OK;
+    const size_t b = 4 * n;
+    if (keys_in != keys_out && overlap(keys_in, b, keys_out, b)) return GC_ERR_INVALID_VALUE;
+    if (vals_in != nullptr) {
+        if (!aligned4(vals_in) || !aligned4(vals_out)) return GC_ERR_MISALIGNED;
+        if (vals_in != vals_out && overlap(vals_in, b, vals_out, b)) return GC_ERR_INVALID_VALUE;
+        const void *keys[2] = {keys_in, keys_out};
+        const void *vals[2] = {vals_in, vals_out};
+        for (const void *k : keys)
+            for (const void *v : vals)
+                if (overlap(k, b, v, b)) return GC_ERR_INVALID_VALUE;
+        if (overlap(ws, ws_bytes, vals_in, b) || overlap(ws, ws_bytes, vals_out, b))
+            return GC_ERR_INVALID_VALUE;
+    }
+    return GC_OK;
+}
+
 gc_status select_like(bool atomic, const void *d_in, void *d_out, uint32_t *d_count, size_t n,
                       gc_dtype dt, gc_pred p, void *d_ws, size_t ws_bytes, cudaStream_t s,
                       const LaunchOpts &o)
@@ -155,6 +179,9 @@ size_t gc_workspace_bytes(gc_op op, size_t n, gc_dtype dtype)
     case GC_OP_SELECT_IF_ATOMIC:
         if (!valid_dtype(dtype)) return 0;
         return kHeaderBytes + status;
+    case GC_OP_RADIX_SORT:
+        if (!valid_dtype(dtype)) return 0;
+        return radix_temp_offset(n) + 2 * radix_temp_stride(n);
     case GC_OP_SPLIT_RADIX:
         return radix_temp_offset(n) + 2 * radix_temp_stride(n);
     }
@@ -168,7 +195,8 @@ size_t gc_tile_elements(gc_op op)
     case GC_OP_INCLUSIVE_SCAN: return scan_tile_elems();
     case GC_OP_SELECT_IF: return select_tile_elems();
     case GC_OP_PARTITION: return partition_tile_elems();
-    case GC_OP_SPLIT_RADIX: return split_tile_elems();
+    case GC_OP_SPLIT_RADIX:
+    case GC_OP_RADIX_SORT: return split_tile_elems();
     case GC_OP_SELECT_IF_ATOMIC: return atomic_tile_elems();
     }
     return 0;
@@ -341,25 +369,30 @@ gc_status gc_split_radix(const uint32_t *d_keys_in, const uint32_t *d_vals_in,
     gc_status st = check_common(d_keys_in, d_keys_out, n, d_ws, ws_bytes, GC_OP_SPLIT_RADIX, GC_U32);
     if (st != GC_OK) return st;
     if (begin_bit < 0 || end_bit > 32 || begin_bit > end_bit) return GC_ERR_INVALID_VALUE;
-    if ((d_vals_in == nullptr) != (d_vals_out == nullptr)) return GC_ERR_INVALID_VALUE;
+    if ((st = check_radix_arrays(d_keys_in, d_vals_in, d_keys_out, d_vals_out, n, d_ws, ws_bytes)) != GC_OK)
+        return st;
     if (n == 0) return GC_OK;
-    const size_t b = 4 * n;
-    if (d_keys_in != d_keys_out && overlap(d_keys_in, b, d_keys_out, b)) return GC_ERR_INVALID_VALUE;
-    if (d_vals_in != nullptr) {
-        if (!aligned4(d_vals_in) || !aligned4(d_vals_out)) return GC_ERR_MISALIGNED;
-        if (d_vals_in != d_vals_out && overlap(d_vals_in, b, d_vals_out, b))
-            return GC_ERR_INVALID_VALUE;
-        const void *keys[2] = {d_keys_in, d_keys_out};
-        const void *vals[2] = {d_vals_in, d_vals_out};
-        for (const void *k : keys)
-            for (const void *v : vals)
-                if (overlap(k, b, v, b)) return GC_ERR_INVALID_VALUE;
-        if (overlap(d_ws, ws_bytes, d_vals_in, b) || overlap(d_ws, ws_bytes, d_vals_out, b))
-            return GC_ERR_INVALID_VALUE;
-    }
     return from_cuda(launch_split_radix(d_keys_in, d_vals_in, d_keys_out, d_vals_out, uint32_t(n),
                                         begin_bit, end_bit, static_cast<uint8_t *>(d_ws), stream,
                                         LaunchOpts{}));
+}
+
+gc_status gc_radix_sort(const void *d_keys_in, const uint32_t *d_vals_in, void *d_keys_out,
+                        uint32_t *d_vals_out, size_t n, gc_dtype dtype, void *d_ws, size_t ws_bytes,
+                        cudaStream_t stream)
+{
+    gc_status st = check_common(d_keys_in, d_keys_out, n, d_ws, ws_bytes, GC_OP_RADIX_SORT, dtype);
+    if (st != GC_OK) return st;
+    if ((st = check_radix_arrays(d_keys_in, d_vals_in, d_keys_out, d_vals_out, n, d_ws, ws_bytes)) != GC_OK)
+        return st;
+    if (n == 0) return GC_OK;
+    // Order-preserving key x ^ (signfill(x) & neg) ^ flip (PredKeyBitClear).
+    const uint32_t neg = dtype == GC_F32 ? 0x7FFFFFFFu : 0u;
+    const uint32_t flip = dtype == GC_U32 ? 0u : 0x80000000u;
+    return from_cuda(launch_split_radix(static_cast<const uint32_t *>(d_keys_in), d_vals_in,
+                                        static_cast<uint32_t *>(d_keys_out), d_vals_out, uint32_t(n),
+                                        0, 32, static_cast<uint8_t *>(d_ws), stream, LaunchOpts{},
+                                        neg, flip));
 }
 
 gc_status gc_query_device_status(void *d_ws, cudaStream_t stream)

@@ -304,6 +304,21 @@ struct PredBitClear {
     __device__ __forceinline__ bool operator()(uint32_t x) const { return ((x >> bit) & 1u) == 0u; }
 };
 
+// Radix split on an order-preserving key of typed bits: key(x) = x ^
+// (signfill(x) & neg) ^ flip ascends with the value, for int32 (neg 0, flip
+// 2^31) and for float32 in IEEE 754 totalOrder (neg 2^31 - 1, flip 2^31: a
+// negative pattern is inverted, a positive one gets its sign bit set).
+// "Bit b of key(x) is clear" goes first; want is bit b of flip, so the key
+// itself is never formed.
+struct PredKeyBitClear {
+    uint32_t bit, neg, want;
+    __device__ __forceinline__ bool operator()(uint32_t x) const
+    {
+        const uint32_t sfill = uint32_t(int32_t(x) >> 31);
+        return (((x ^ (sfill & neg)) >> bit) & 1u) == want;
+    }
+};
+
 // ---------------------------------------------------------------- tile geometry
 //
 // A tile is ROWS rows of THREADS x 4 consecutive elements.  Thread t owns the

@@ -155,7 +155,8 @@ cudaError_t launch_partition(const void *in, void *out, uint32_t *count_true, ui
                              const LaunchOpts &o);
 cudaError_t launch_split_radix(const uint32_t *keys_in, const uint32_t *vals_in,
                                uint32_t *keys_out, uint32_t *vals_out, uint32_t n, int begin_bit,
-                               int end_bit, uint8_t *ws, cudaStream_t s, const LaunchOpts &o);
+                               int end_bit, uint8_t *ws, cudaStream_t s, const LaunchOpts &o,
+                               uint32_t key_neg = 0u, uint32_t key_flip = 0u);
 
 uint32_t scan_tile_elems();
 uint32_t select_tile_elems();

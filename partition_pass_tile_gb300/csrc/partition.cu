@@ -43,7 +43,7 @@ partition_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__restric
 
     const uint32_t tile = claim_tile(ws, &s_tile);
     if (tile >= num_tiles) return;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const uint32_t base = tile * uint32_t(TT::kElems);
 
     uint32_t x[ROWS][4];
@@ -173,9 +173,13 @@ count_kernel(const uint32_t *__restrict__ in, uint32_t n, Pred pred, uint8_t *ws
 // before a byte can overflow.  Reduced across the warp with a butterfly
 // that leaves bit b's total in lane b, then across the CTA and the grid as in
 // count_kernel; the last CTA stores n - ones as the clear-bit count.
-template <int THREADS, bool VEC>
+// KEYED counts the bits of the order-preserving key x ^ (signfill(x) & neg)
+// ^ flip instead of x (see PredKeyBitClear); the padding past n loads as 0,
+// whose key is flip, and the last CTA takes those bits back out.
+template <int THREADS, bool VEC, bool KEYED>
 __global__ void __launch_bounds__(THREADS)
-bit_histogram_kernel(const uint32_t *__restrict__ keys, uint32_t n, uint8_t *ws)
+bit_histogram_kernel(const uint32_t *__restrict__ keys, uint32_t n, uint8_t *ws, uint32_t neg,
+                     uint32_t flip)
 {
     __shared__ uint32_t s_ones[32];
     const int lane = threadIdx.x & 31;
@@ -195,6 +199,10 @@ bit_histogram_kernel(const uint32_t *__restrict__ keys, uint32_t n, uint8_t *ws)
     for (uint32_t v = blockIdx.x * THREADS + threadIdx.x; v < nvec; v += stride) {
         uint32_t x[4];
         load4<VEC>(keys, 4u * v, n, 0u, x);  // padding keys are 0: no bits set
+        if (KEYED) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) x[k] ^= (uint32_t(int32_t(x[k]) >> 31) & neg) ^ flip;
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
 #pragma unroll
@@ -243,7 +251,8 @@ bit_histogram_kernel(const uint32_t *__restrict__ keys, uint32_t n, uint8_t *ws)
     __syncthreads();
     if (s_ones[0] != 0u && threadIdx.x < 32) {
         __threadfence();
-        const uint32_t total_ones = atomicExch(hdr_u32(ws, kHdrBitAcc + 4u * threadIdx.x), 0u);
+        uint32_t total_ones = atomicExch(hdr_u32(ws, kHdrBitAcc + 4u * threadIdx.x), 0u);
+        if (KEYED) total_ones -= (4u * ((n + 3u) / 4u) - n) * ((flip >> threadIdx.x) & 1u);
         *hdr_u32(ws, kHdrBitZeros + 4u * threadIdx.x) = n - total_ones;
         if (threadIdx.x == 0) atomicExch(hdr_u32(ws, kHdrReduceCtr), 0u);
     }
@@ -384,8 +393,10 @@ cudaError_t launch_partition_cmp(const void *in, void *out, uint32_t *count_true
 
 cudaError_t launch_split_radix(const uint32_t *keys_in, const uint32_t *vals_in,
                                uint32_t *keys_out, uint32_t *vals_out, uint32_t n, int begin_bit,
-                               int end_bit, uint8_t *ws, cudaStream_t s, const LaunchOpts &o)
+                               int end_bit, uint8_t *ws, cudaStream_t s, const LaunchOpts &o,
+                               uint32_t key_neg, uint32_t key_flip)
 {
+    const bool keyed = (key_neg | key_flip) != 0u;
     const bool vals = vals_in != nullptr;
     const int passes = end_bit - begin_bit;
     cudaError_t e;
@@ -401,10 +412,17 @@ cudaError_t launch_split_radix(const uint32_t *keys_in, const uint32_t *vals_in,
     constexpr int RT = kReduceThreads;
     const int grid = reduce_grid(n, RT);
     if ((e = clear_accumulators(ws, s)) != cudaSuccess) return e;
-    if (aligned16(keys_in))
-        bit_histogram_kernel<RT, true><<<grid, RT, 0, s>>>(keys_in, n, ws);
-    else
-        bit_histogram_kernel<RT, false><<<grid, RT, 0, s>>>(keys_in, n, ws);
+    if (keyed) {
+        if (aligned16(keys_in))
+            bit_histogram_kernel<RT, true, true><<<grid, RT, 0, s>>>(keys_in, n, ws, key_neg, key_flip);
+        else
+            bit_histogram_kernel<RT, false, true><<<grid, RT, 0, s>>>(keys_in, n, ws, key_neg, key_flip);
+    } else {
+        if (aligned16(keys_in))
+            bit_histogram_kernel<RT, true, false><<<grid, RT, 0, s>>>(keys_in, n, ws, 0u, 0u);
+        else
+            bit_histogram_kernel<RT, false, false><<<grid, RT, 0, s>>>(keys_in, n, ws, 0u, 0u);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     uint32_t *tmp_k = reinterpret_cast<uint32_t *>(ws + radix_temp_offset(n));
@@ -427,9 +445,15 @@ cudaError_t launch_split_radix(const uint32_t *keys_in, const uint32_t *vals_in,
         uint32_t *dst_v = vals ? (to_out ? vals_out : tmp_v) : nullptr;
         const int bit = begin_bit + p;
         const uint32_t *T = reinterpret_cast<const uint32_t *>(ws + kHdrBitZeros + 4 * bit);
-        const gcd::PredBitClear pred{uint32_t(bit)};
-        e = vals ? run_partition_pass<gcd::PredBitClear, true>(src_k, src_v, dst_k, dst_v, n, T, pred, ws, s, o, true)
-                 : run_partition_pass<gcd::PredBitClear, false>(src_k, nullptr, dst_k, nullptr, n, T, pred, ws, s, o, true);
+        if (keyed) {
+            const gcd::PredKeyBitClear pred{uint32_t(bit), key_neg, (key_flip >> bit) & 1u};
+            e = vals ? run_partition_pass<gcd::PredKeyBitClear, true>(src_k, src_v, dst_k, dst_v, n, T, pred, ws, s, o, true)
+                     : run_partition_pass<gcd::PredKeyBitClear, false>(src_k, nullptr, dst_k, nullptr, n, T, pred, ws, s, o, true);
+        } else {
+            const gcd::PredBitClear pred{uint32_t(bit)};
+            e = vals ? run_partition_pass<gcd::PredBitClear, true>(src_k, src_v, dst_k, dst_v, n, T, pred, ws, s, o, true)
+                     : run_partition_pass<gcd::PredBitClear, false>(src_k, nullptr, dst_k, nullptr, n, T, pred, ws, s, o, true);
+        }
         if (e != cudaSuccess) return e;
         src_k = dst_k;
         src_v = dst_v;

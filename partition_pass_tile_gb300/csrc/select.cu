@@ -42,7 +42,7 @@ select_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, uint3
 
     const uint32_t tile = claim_tile(ws, &s_tile);
     if (tile >= num_tiles) return;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const uint32_t base = tile * uint32_t(TT::kElems);
 
     uint32_t x[ROWS][4];

@@ -25,6 +25,7 @@ I32, U32, F32 = 0, 1, 2
 NONZERO, ODD, EVEN = 0, 1, 2
 OP_EXCLUSIVE_SCAN, OP_SELECT_IF, OP_PARTITION, OP_SPLIT_RADIX, OP_SELECT_IF_ATOMIC = range(5)
 OP_INCLUSIVE_SCAN = 5
+OP_RADIX_SORT = 6
 LT, LE, GT, GE, EQ, NE, MASK_EQ, MASK_NE = range(8)
 CMP_NAMES = {"<": LT, "<=": LE, ">": GT, ">=": GE, "==": EQ, "!=": NE,
              "mask==": MASK_EQ, "mask!=": MASK_NE}
@@ -75,6 +76,7 @@ def load(path: str | Path | None = None) -> ctypes.CDLL:
         "gc_inclusive_scan": ([V, V, V, Z, I, V, Z, V], S),
         "gc_select_if_pred": ([V, V, V, Z, I, ctypes.POINTER(Predicate), V, Z, V], S),
         "gc_partition_pred": ([V, V, V, Z, I, ctypes.POINTER(Predicate), V, Z, V], S),
+        "gc_radix_sort": ([V, V, V, V, Z, I, V, Z, V], S),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -279,6 +281,25 @@ def split_radix(keys: torch.Tensor, vals: torch.Tensor | None = None, begin_bit:
     _check(load().gc_split_radix(_ptr(keys), _ptr(vals), _ptr(keys_out), _ptr(vals_out), n,
                                  begin_bit, end_bit, _ptr(ws), ws.numel(), _stream(stream)),
            "gc_split_radix")
+    return keys_out, vals_out
+
+
+def radix_sort(keys: torch.Tensor, vals: torch.Tensor | None = None,
+               keys_out: torch.Tensor | None = None, vals_out: torch.Tensor | None = None,
+               ws: torch.Tensor | None = None, stream=None):
+    """-> (keys_out, vals_out): stable ascending sort in keys' dtype order (float32:
+    IEEE 754 totalOrder), 32-bit payloads carried."""
+    n = keys.numel()
+    dt = dtype_code(keys)
+    if vals is not None and vals.element_size() != 4:
+        raise TypeError("radix_sort carries 32-bit payloads")
+    if keys_out is None:
+        keys_out = torch.empty_like(keys)
+    if vals is not None and vals_out is None:
+        vals_out = torch.empty_like(vals)
+    ws = _ws(ws, OP_RADIX_SORT, n, dt, keys.device)
+    _check(load().gc_radix_sort(_ptr(keys), _ptr(vals), _ptr(keys_out), _ptr(vals_out), n, dt,
+                                _ptr(ws), ws.numel(), _stream(stream)), "gc_radix_sort")
     return keys_out, vals_out
 
 

@@ -38,7 +38,7 @@ def test_header_declares_the_entry_points():
                  "gc_select_if_atomic", "gc_workspace_bytes", "gc_query_device_status",
                  "gc_status_string", "gc_workspace_init", "gc_tile_elements",
                  "gc_testing_select_if_skip_tile0", "gc_inclusive_scan", "gc_select_if_pred",
-                 "gc_partition_pred", "gc_select_if_noalloc"]:
+                 "gc_partition_pred", "gc_select_if_noalloc", "gc_radix_sort"]:
         assert want in names
 
 
@@ -171,6 +171,33 @@ def test_radix_validation(lib):
     assert call(vi=V1 + 2) == E["GC_ERR_MISALIGNED"]
     assert call(wsb=1 << 12) == E["GC_ERR_WORKSPACE_TOO_SMALL"]
     assert call(n=2 ** 31) == E["GC_ERR_INVALID_VALUE"]
+
+
+def test_radix_sort_validation(lib):
+    E = {v: k for k, v in gc.STATUS.items()}
+    f = lib.gc_radix_sort
+    K2, V1, V2 = 0x50000000, 0x60000000, 0x70000000
+    ok = dict(ki=IN, vi=V1, ko=K2, vo=V2, n=1000, dt=gc.F32, ws=WS, wsb=BIG)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["ki"], a["vi"], a["ko"], a["vo"], a["n"], a["dt"], a["ws"], a["wsb"], None)
+    assert call(dt=3) == E["GC_ERR_INVALID_VALUE"]
+    assert call(dt=-1) == E["GC_ERR_INVALID_VALUE"]
+    assert call(vi=None) == E["GC_ERR_INVALID_VALUE"]
+    assert call(vo=None) == E["GC_ERR_INVALID_VALUE"]
+    assert call(vo=IN + 64) == E["GC_ERR_INVALID_VALUE"]
+    assert call(ko=IN + 8) == E["GC_ERR_INVALID_VALUE"]
+    assert call(ki=IN + 2) == E["GC_ERR_MISALIGNED"]
+    assert call(vi=V1 + 2) == E["GC_ERR_MISALIGNED"]
+    assert call(wsb=1 << 12) == E["GC_ERR_WORKSPACE_TOO_SMALL"]
+    assert call(n=2 ** 31) == E["GC_ERR_INVALID_VALUE"]
+    assert call(ws=None) == E["GC_ERR_INVALID_VALUE"]
+    for dt in (gc.I32, gc.U32, gc.F32):
+        assert (lib.gc_workspace_bytes(gc.OP_RADIX_SORT, 12345, dt)
+                == lib.gc_workspace_bytes(gc.OP_SPLIT_RADIX, 12345, gc.U32))
+    assert lib.gc_workspace_bytes(gc.OP_RADIX_SORT, 12345, 7) == 0
+    assert lib.gc_tile_elements(gc.OP_RADIX_SORT) == lib.gc_tile_elements(gc.OP_SPLIT_RADIX)
 
 
 def test_binding_refuses_cpu_tensors(lib):

@@ -133,3 +133,70 @@ def test_pred_at_scale(orc):
     want, t = orc.partition_cmp(xi, O.LT, -(2 ** 30))
     out, ct = gc.partition_pred(dev(xi), gc.predicate(torch.zeros(1, dtype=torch.int32), "<", -(2 ** 30)))
     assert int(host(ct)[0]) == t and np.array_equal(host(out), want)
+
+
+# ---------------------------------------------------------------- typed radix sort
+
+def radix_input(n, dt, seed):
+    rng = np.random.default_rng(seed)
+    if dt == gc.I32:
+        x = rng.integers(-2 ** 31, 2 ** 31, size=n, dtype=np.int64).astype(np.int32)
+        x[::17] = rng.integers(-3, 4, size=x[::17].shape[0])  # many duplicates around 0
+        x[5::31] = np.iinfo(np.int32).min
+        x[6::37] = np.iinfo(np.int32).max
+    elif dt == gc.U32:
+        x = rng.integers(0, 2 ** 32, size=n, dtype=np.uint64).astype(np.uint32)
+        x[::13] = 7
+    else:
+        x = (rng.standard_normal(n) * 1e3).astype(np.float32)
+        sp = np.array([0x00000000, 0x80000000, 0x7FC00000, 0xFFC00000, 0x7F800001, 0xFF800001,
+                       0x7F800000, 0xFF800000, 0x00000001, 0x80000001, 0x3F800000, 0xBF800000],
+                      dtype=np.uint32).view(np.float32)
+        x[::6] = sp[rng.integers(0, sp.shape[0], size=x[::6].shape[0])]
+    return x
+
+
+@pytest.mark.parametrize("dt", [gc.I32, gc.U32, gc.F32])
+@pytest.mark.parametrize("offset,with_vals", [(0, True), (0, False), (1, True)])
+def test_radix_sort_sizes(orc, dt, offset, with_vals):
+    for n in sizes(gc.OP_RADIX_SORT):
+        x = radix_input(n, dt, n + 7 * dt)
+        vals = np.arange(n, dtype=np.uint32) if with_vals else None
+        wk, wv = orc.radix_sort(x, vals)
+        kd = dev(x, offset)
+        vd = dev(vals, offset) if with_vals else None
+        ko, vo = gc.radix_sort(kd, vd, keys_out=empty_like_offset(kd, offset),
+                               vals_out=empty_like_offset(vd, offset) if with_vals else None)
+        assert np.array_equal(host(ko).view(np.uint32), wk.view(np.uint32)), (n, dt)
+        if with_vals:
+            assert np.array_equal(host(vo), wv), (n, dt)
+
+
+@pytest.mark.parametrize("dt", [gc.I32, gc.F32])
+def test_radix_sort_in_place_and_order(orc, dt):
+    n = 3 * gc.tile_elements(gc.OP_RADIX_SORT) + 5
+    x = radix_input(n, dt, 99)
+    vals = np.arange(n, dtype=np.uint32)
+    kd, vd = dev(x), dev(vals)
+    gc.radix_sort(kd, vd, keys_out=kd, vals_out=vd)  # in place
+    wk, wv = orc.radix_sort(x, vals)
+    got_k, got_v = host(kd), host(vd)
+    assert np.array_equal(got_k.view(np.uint32), wk.view(np.uint32))
+    assert np.array_equal(got_v, wv)
+    assert np.array_equal(x[got_v].view(np.uint32), got_k.view(np.uint32))
+    if dt == gc.I32:
+        assert np.all(got_k[1:] >= got_k[:-1])
+    else:
+        finite = got_k[~np.isnan(got_k)]
+        assert np.all(finite[1:] >= finite[:-1])
+
+
+def test_radix_sort_float_at_scale(orc):
+    """2^26 float32 keys (normal, with specials), index payload: every element compared."""
+    n = 1 << 26
+    x = radix_input(n, gc.F32, 2026)
+    vals = np.arange(n, dtype=np.uint32)
+    wk, wv = orc.radix_sort(x, vals)
+    ko, vo = gc.radix_sort(dev(x), dev(vals))
+    assert np.array_equal(host(ko).view(np.uint32), wk.view(np.uint32))
+    assert np.array_equal(host(vo), wv)
