@@ -90,6 +90,13 @@ constexpr int kPartPipeThreads = GC_PART_PIPE_THREADS, kPartPipeRows = GC_PART_P
 constexpr int kPartPipeStages = GC_PART_PIPE_STAGES;
 constexpr int kSplitPipeThreads = GC_SPLIT_PIPE_THREADS, kSplitPipeRows = GC_SPLIT_PIPE_ROWS;
 constexpr int kSplitPipeStages = GC_SPLIT_PIPE_STAGES;
+// Minimum resident CTAs per SM the persistent kernels are compiled for
+// (the second __launch_bounds__ argument); 0 leaves it out, which lets ptxas
+// pick its own register budget for the block size.
+#ifndef GC_PIPE_MIN_BLOCKS
+#define GC_PIPE_MIN_BLOCKS 0
+#endif
+constexpr int kPipeMinBlocks = GC_PIPE_MIN_BLOCKS;
 
 
 constexpr int kScanThreads = GC_SCAN_THREADS, kScanRows = GC_SCAN_ROWS;

@@ -9,8 +9,14 @@
 
 namespace gcd {
 
+#if GC_PIPE_MIN_BLOCKS > 0
+#define GC_PIPE_BOUNDS(T) __launch_bounds__(T, GC_PIPE_MIN_BLOCKS)
+#else
+#define GC_PIPE_BOUNDS(T) __launch_bounds__(T)
+#endif
+
 template <int THREADS, int STAGES, class Op>
-__global__ void __launch_bounds__(THREADS)
+__global__ void GC_PIPE_BOUNDS(THREADS)
 pipeline_kernel(Op op, uint32_t n, uint32_t num_tiles, uint8_t *ws, uint64_t timeout_ns)
 {
     extern __shared__ __align__(128) uint8_t smem[];

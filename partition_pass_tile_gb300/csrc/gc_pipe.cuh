@@ -89,6 +89,54 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16) from shared src to global dst
+// (both 16-byte aligned), in the current bulk group of this thread.
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(dst), "r"(smem_addr(src)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Until every bulk store this thread committed has read its shared source.
+__device__ __forceinline__ void bulk_wait_read_all()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;");
+}
+
+// Until every bulk store this thread committed is complete.
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Writes s[soff .. soff + len) to out[dst .. dst + len) when soff and dst
+// agree modulo 4 elements (16 bytes) and out is 16-byte aligned: the
+// aligned middle of the run goes out as one bulk copy issued by thread 0,
+// the ragged head and tail (at most 3 elements each) as plain stores by
+// threads 0-2 and 32-34.  The caller has made the run's shared-memory writes
+// visible to the async proxy (fence.proxy.async by every writer, then a
+// barrier) and commits thread 0's bulk group afterwards.
+template <int THREADS>
+__device__ __forceinline__ void store_run_bulk(uint32_t *__restrict__ out, uint32_t dst,
+                                               const uint32_t *s, uint32_t soff, uint32_t len)
+{
+    static_assert(THREADS >= 64, "head and tail threads");
+    if (len == 0u) return;
+    const uint32_t end = dst + len;
+    const uint32_t a = min((dst + 3u) & ~3u, end);
+    const uint32_t b = max(end & ~3u, a);
+    const uint32_t tid = threadIdx.x;
+    if (tid < a - dst) __stcs(out + dst + tid, s[soff + tid]);
+    if (tid >= 32u && tid - 32u < end - b) __stcs(out + b + (tid - 32u), s[soff + (b - dst) + (tid - 32u)]);
+    if (tid == 0u && b > a) bulk_store(out + a, s + soff + (a - dst), (b - a) * 4u);
+}
+
 // Waits for a stage's phase.  The wait is bounded: past timeout_ns of device
 // time it records GC_ERR_TIMEOUT and returns, and the caller carries on with
 // whatever the buffer holds (every thread follows the same path afterwards,

@@ -196,12 +196,16 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
                     op.template finish<false>(pipe, ps, prev, pbase, pstaged, n, prefix, prev_agg, last, prv, ld);
             }
             __syncthreads();  // the previous tile's stage is free again
-            if (tid == 0) pipe.refill(ps, op.srcs, prev, TE, n, num_tiles);
+            if (tid == 0) {
+                bulk_wait_read_all();  // ... once its bulk stores have read it
+                pipe.refill(ps, op.srcs, prev, TE, n, num_tiles);
+            }
         }
         if (!have) break;
         prev_agg = agg;
         prv = cur;
     }
+    if (tid == 0) bulk_wait_all();  // shared memory stays until the stores are done
 }
 
 // Grid limit of pipeline_run: the window of a tile must fit kWinPerThread
@@ -456,8 +460,15 @@ struct SelectOp {
             for (int q = 0; q < 4; ++q)
                 if ((c.mask[r] >> q) & 1u) buf[pos++] = ld.x[r][q];
         }
-        __syncthreads();
-        store_run<THREADS, VEC>(out, before, buf, shift, kept);
+        if (VEC) {
+            fence_proxy_async_smem();
+            __syncthreads();
+            store_run_bulk<THREADS>(out, before, buf, shift, kept);
+            if (threadIdx.x == 0) bulk_commit();
+        } else {
+            __syncthreads();
+            store_run<THREADS, VEC>(out, before, buf, shift, kept);
+        }
         if (threadIdx.x == 0 && last) *count = before + kept;
         (void)tile;
     }
@@ -594,12 +605,25 @@ struct PartitionOp {
                 }
             }
         }
-        __syncthreads();
-        store_run<THREADS, VEC>(keys_out, dst_kept, kbuf, sh_kept, kept_len);
-        store_run<THREADS, VEC>(keys_out, dst_rej, kbuf, sh_rej, rejected);
-        if (VALS) {
-            store_run<THREADS, VEC>(vals_out, dst_kept, vbuf, sh_kept, kept_len);
-            store_run<THREADS, VEC>(vals_out, dst_rej, vbuf, sh_rej, rejected);
+        if (VEC) {
+            // The runs leave by bulk copies from the stage buffer(s).
+            fence_proxy_async_smem();
+            __syncthreads();
+            store_run_bulk<THREADS>(keys_out, dst_kept, kbuf, sh_kept, kept_len);
+            store_run_bulk<THREADS>(keys_out, dst_rej, kbuf, sh_rej, rejected);
+            if (VALS) {
+                store_run_bulk<THREADS>(vals_out, dst_kept, vbuf, sh_kept, kept_len);
+                store_run_bulk<THREADS>(vals_out, dst_rej, vbuf, sh_rej, rejected);
+            }
+            if (tid == 0) bulk_commit();
+        } else {
+            __syncthreads();
+            store_run<THREADS, VEC>(keys_out, dst_kept, kbuf, sh_kept, kept_len);
+            store_run<THREADS, VEC>(keys_out, dst_rej, kbuf, sh_rej, rejected);
+            if (VALS) {
+                store_run<THREADS, VEC>(vals_out, dst_kept, vbuf, sh_kept, kept_len);
+                store_run<THREADS, VEC>(vals_out, dst_rej, vbuf, sh_rej, rejected);
+            }
         }
         (void)last;
     }
