@@ -115,6 +115,11 @@ __device__ __forceinline__ void bulk_wait_all()
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Shortest run worth a bulk store: below it the proxy fence and the wait for
+// the bulk group before the stage is refilled cost more than the threads'
+// own 128-bit stores.
+constexpr uint32_t kBulkMinRun = 512u;
+
 // Writes s[soff .. soff + len) to out[dst .. dst + len) when soff and dst
 // agree modulo 4 elements (16 bytes) and out is 16-byte aligned: the
 // aligned middle of the run goes out as one bulk copy issued by thread 0,

@@ -460,7 +460,7 @@ struct SelectOp {
             for (int q = 0; q < 4; ++q)
                 if ((c.mask[r] >> q) & 1u) buf[pos++] = ld.x[r][q];
         }
-        if (VEC) {
+        if (VEC && kept >= kBulkMinRun) {
             fence_proxy_async_smem();
             __syncthreads();
             store_run_bulk<THREADS>(out, before, buf, shift, kept);
@@ -605,7 +605,7 @@ struct PartitionOp {
                 }
             }
         }
-        if (VEC) {
+        if (VEC && valid >= kBulkMinRun) {
             // The runs leave by bulk copies from the stage buffer(s).
             fence_proxy_async_smem();
             __syncthreads();

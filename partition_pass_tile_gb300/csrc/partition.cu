@@ -166,16 +166,30 @@ count_kernel(const uint32_t *__restrict__ in, uint32_t n, Pred pred, uint8_t *ws
     }
 }
 
-// Radix histogram: for every bit b, how many keys have it set.  Counted
-// eight bits at a time in byte lanes: (x >> j) & 0x01010101 holds bits j,
-// j+8, j+16, j+24 as four byte-wide 0/1 values, so eight 32-bit accumulators
-// count all 32 bits, and are spilled into 32 wide counters every 255 keys
-// before a byte can overflow.  Reduced across the warp with a butterfly
-// that leaves bit b's total in lane b, then across the CTA and the grid as in
-// count_kernel; the last CTA stores n - ones as the clear-bit count.
+// Carry-save adder: l + 2h = a + b + c, bit by bit.
+__device__ __forceinline__ void csa(uint32_t &h, uint32_t &l, uint32_t a, uint32_t b, uint32_t c)
+{
+    const uint32_t u = a ^ b;
+    h = (a & b) | (u & c);
+    l = u ^ c;
+}
+
+// Radix histogram: for every bit b, how many keys have it set.  Keys are
+// counted eight at a time in bit-sliced form (the carry-save tree of the
+// Harley-Seal population count): seven adders fold eight keys into the
+// running ones, twos and fours words and one "eights" word, whose bit b says
+// that eight more keys have bit b set.  Only that word is spread into
+// per-bit counters, eight bits at a time in byte lanes ((w >> j) &
+// 0x01010101 holds bits j, j+8, j+16, j+24 as four byte-wide 0/1 values),
+// spilled into 32 wide counters every 255 groups before a byte can
+// overflow; the ones, twos and fours words are added in at the end.
+// Reduced across the warp with a butterfly that leaves bit b's total in
+// lane b, then across the CTA and the grid as in count_kernel; the last CTA
+// stores n - ones as the clear-bit count.
 // KEYED counts the bits of the order-preserving key x ^ (signfill(x) & neg)
-// ^ flip instead of x (see PredKeyBitClear); the padding past n loads as 0,
-// whose key is flip, and the last CTA takes those bits back out.
+// ^ flip instead of x (see PredKeyBitClear); the padding past n in the last
+// vector loads as 0, whose key is flip, and the last CTA takes those bits
+// back out.
 template <int THREADS, bool VEC, bool KEYED>
 __global__ void __launch_bounds__(THREADS)
 bit_histogram_kernel(const uint32_t *__restrict__ keys, uint32_t n, uint8_t *ws, uint32_t neg,
@@ -192,28 +206,41 @@ bit_histogram_kernel(const uint32_t *__restrict__ keys, uint32_t n, uint8_t *ws,
     uint32_t acc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0u;
-    uint32_t in_acc = 0;  // keys added to acc since the last spill (<= 255)
+    uint32_t in_acc = 0;  // eights words added to acc since the last spill (<= 255)
+    uint32_t w1 = 0u, w2 = 0u, w4 = 0u;  // bit-sliced counts 0..7 per bit position
 
     const uint32_t nvec = (n + 3u) / 4u;
     const uint32_t stride = gridDim.x * THREADS;
-    for (uint32_t v = blockIdx.x * THREADS + threadIdx.x; v < nvec; v += stride) {
-        uint32_t x[4];
+    for (uint32_t v = blockIdx.x * THREADS + threadIdx.x; v < nvec; v += 2u * stride) {
+        uint32_t x[4], y[4];
         load4<VEC>(keys, 4u * v, n, 0u, x);  // padding keys are 0: no bits set
+        const bool have_y = v + stride < nvec;
+        if (have_y)
+            load4<VEC>(keys, 4u * (v + stride), n, 0u, y);
+        else
+            y[0] = y[1] = y[2] = y[3] = 0u;
         if (KEYED) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) x[k] ^= (uint32_t(int32_t(x[k]) >> 31) & neg) ^ flip;
+            for (int k = 0; k < 4; ++k) {
+                x[k] ^= (uint32_t(int32_t(x[k]) >> 31) & neg) ^ flip;
+                y[k] = have_y ? y[k] ^ ((uint32_t(int32_t(y[k]) >> 31) & neg) ^ flip) : 0u;
+            }
         }
+        uint32_t t2a, t2b, t4a, t4b, w8;
+        csa(t2a, w1, w1, x[0], x[1]);
+        csa(t2b, w1, w1, x[2], x[3]);
+        csa(t4a, w2, w2, t2a, t2b);
+        csa(t2a, w1, w1, y[0], y[1]);
+        csa(t2b, w1, w1, y[2], y[3]);
+        csa(t4b, w2, w2, t2a, t2b);
+        csa(w8, w4, w4, t4a, t4b);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] += (x[k] >> j) & 0x01010101u;
-        }
-        in_acc += 4;
-        if (in_acc > 251) {
+        for (int j = 0; j < 8; ++j) acc[j] += (w8 >> j) & 0x01010101u;
+        if (++in_acc == 255u) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) ones[8 * q + j] += (acc[j] >> (8 * q)) & 0xffu;
+                for (int q = 0; q < 4; ++q) ones[8 * q + j] += 8u * ((acc[j] >> (8 * q)) & 0xffu);
                 acc[j] = 0u;
             }
             in_acc = 0;
@@ -222,7 +249,10 @@ bit_histogram_kernel(const uint32_t *__restrict__ keys, uint32_t n, uint8_t *ws,
 #pragma unroll
     for (int j = 0; j < 8; ++j)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) ones[8 * q + j] += (acc[j] >> (8 * q)) & 0xffu;
+        for (int q = 0; q < 4; ++q) ones[8 * q + j] += 8u * ((acc[j] >> (8 * q)) & 0xffu);
+#pragma unroll
+    for (int b = 0; b < 32; ++b)
+        ones[b] += ((w1 >> b) & 1u) + 2u * ((w2 >> b) & 1u) + 4u * ((w4 >> b) & 1u);
 
     // Butterfly reduce-scatter: after the step with offset o each lane keeps
     // the half of its array selected by (lane & o); at the end lane l holds
