@@ -365,8 +365,10 @@ def run_gc(args):
 
     # The widened entry points (not part of the step): inclusive scans, the
     # parameterised-predicate select / partition and the float32-key radix sort
-    # (32 splits over the order-preserving key, payload carried) on the same
-    # 2^28 arrays.
+    # (four 8-bit digit passes over the order-preserving key, payload carried;
+    # algorithmic bytes: keys and payloads read and written once per pass) on
+    # the same 2^28 arrays.
+    ws_sort = gc.workspace(gc.OP_RADIX_SORT, n, gc.F32, dev)
     pf = gc.predicate(d["f"], ">", 0.75)
     pi = gc.predicate(d["x"], "<", 0)
     next_calls = {
@@ -374,7 +376,7 @@ def run_gc(args):
         "inclusive_scan_f32": (lambda: gc.inclusive_scan(d["f"], out=outf, total=counts[1:2].view(torch.float32), ws=ws, stream=stream), 8.0 * n),
         "select_pred_f32_gt_0.75": (lambda: gc.select_if_pred(d["f"], pf, out=out_a, count=counts[2:3], ws=ws, stream=stream), None),
         "partition_pred_i32_lt_0": (lambda: gc.partition_pred(d["x"], pi, out=out_a, count_true=counts[5:6], ws=ws, stream=stream), 8.0 * n + 4),
-        "radix_sort_f32": (lambda: gc.radix_sort(d["f"], d["payload"], keys_out=outf, vals_out=out_b.view(torch.uint32), ws=ws, stream=stream), 516.0 * n),
+        "radix_sort_f32": (lambda: gc.radix_sort(d["f"], d["payload"], keys_out=outf, vals_out=out_b.view(torch.uint32), ws=ws_sort, stream=stream), 64.0 * n),
     }
     next_ops = {}
     for name, (fn, nbytes) in next_calls.items():

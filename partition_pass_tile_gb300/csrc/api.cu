@@ -181,7 +181,7 @@ size_t gc_workspace_bytes(gc_op op, size_t n, gc_dtype dtype)
         return kHeaderBytes + status;
     case GC_OP_RADIX_SORT:
         if (!valid_dtype(dtype)) return 0;
-        return radix_temp_offset(n) + 2 * radix_temp_stride(n);
+        return digit_table_offset(n) + digit_table_bytes(n);
     case GC_OP_SPLIT_RADIX:
         return radix_temp_offset(n) + 2 * radix_temp_stride(n);
     }
@@ -195,8 +195,8 @@ size_t gc_tile_elements(gc_op op)
     case GC_OP_INCLUSIVE_SCAN: return scan_tile_elems();
     case GC_OP_SELECT_IF: return select_tile_elems();
     case GC_OP_PARTITION: return partition_tile_elems();
-    case GC_OP_SPLIT_RADIX:
-    case GC_OP_RADIX_SORT: return split_tile_elems();
+    case GC_OP_SPLIT_RADIX: return split_tile_elems();
+    case GC_OP_RADIX_SORT: return kDigitTile;
     case GC_OP_SELECT_IF_ATOMIC: return atomic_tile_elems();
     }
     return 0;
@@ -389,10 +389,10 @@ gc_status gc_radix_sort(const void *d_keys_in, const uint32_t *d_vals_in, void *
     // Order-preserving key x ^ (signfill(x) & neg) ^ flip (PredKeyBitClear).
     const uint32_t neg = dtype == GC_F32 ? 0x7FFFFFFFu : 0u;
     const uint32_t flip = dtype == GC_U32 ? 0u : 0x80000000u;
-    return from_cuda(launch_split_radix(static_cast<const uint32_t *>(d_keys_in), d_vals_in,
-                                        static_cast<uint32_t *>(d_keys_out), d_vals_out, uint32_t(n),
-                                        0, 32, static_cast<uint8_t *>(d_ws), stream, LaunchOpts{},
-                                        neg, flip));
+    return from_cuda(launch_radix_sort_digits(static_cast<const uint32_t *>(d_keys_in), d_vals_in,
+                                              static_cast<uint32_t *>(d_keys_out), d_vals_out,
+                                              uint32_t(n), neg, flip, static_cast<uint8_t *>(d_ws),
+                                              stream, LaunchOpts{}));
 }
 
 gc_status gc_query_device_status(void *d_ws, cudaStream_t stream)

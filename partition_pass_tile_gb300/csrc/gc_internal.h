@@ -125,6 +125,13 @@ inline size_t status_bytes(size_t tiles) { return 8 * tiles; }
 inline size_t max_tiles(size_t n) { return ceil_div(n, kMinTileElems) + 1; }
 inline size_t radix_temp_offset(size_t n) { return align_up(kHeaderBytes + status_bytes(max_tiles(n)), 256); }
 inline size_t radix_temp_stride(size_t n) { return align_up(4 * n, 256); }
+// The digit radix sort: keys per tile of its count and scatter kernels, and
+// its digit-major count table (256 words per tile) after the ping-pong
+// buffers; the scan of that table reports its total in the header.
+constexpr uint32_t kDigitTile = 4096;
+constexpr uint32_t kHdrDigitScanTotal = 320;
+inline size_t digit_table_offset(size_t n) { return radix_temp_offset(n) + 2 * radix_temp_stride(n); }
+inline size_t digit_table_bytes(size_t n) { return align_up(4 * 256 * ceil_div(n, kDigitTile), 256); }
 
 struct LaunchOpts {
     uint64_t timeout_ns = 1000000000ull;  // a look-back wait gives up after this long
@@ -164,6 +171,11 @@ cudaError_t launch_split_radix(const uint32_t *keys_in, const uint32_t *vals_in,
                                uint32_t *keys_out, uint32_t *vals_out, uint32_t n, int begin_bit,
                                int end_bit, uint8_t *ws, cudaStream_t s, const LaunchOpts &o,
                                uint32_t key_neg = 0u, uint32_t key_flip = 0u);
+
+cudaError_t launch_radix_sort_digits(const uint32_t *keys_in, const uint32_t *vals_in,
+                                     uint32_t *keys_out, uint32_t *vals_out, uint32_t n,
+                                     uint32_t key_neg, uint32_t key_flip, uint8_t *ws,
+                                     cudaStream_t s, const LaunchOpts &o);
 
 uint32_t scan_tile_elems();
 uint32_t select_tile_elems();

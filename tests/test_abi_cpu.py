@@ -194,10 +194,13 @@ def test_radix_sort_validation(lib):
     assert call(n=2 ** 31) == E["GC_ERR_INVALID_VALUE"]
     assert call(ws=None) == E["GC_ERR_INVALID_VALUE"]
     for dt in (gc.I32, gc.U32, gc.F32):
-        assert (lib.gc_workspace_bytes(gc.OP_RADIX_SORT, 12345, dt)
-                == lib.gc_workspace_bytes(gc.OP_SPLIT_RADIX, 12345, gc.U32))
+        # the ping-pong buffers of the split sort plus a 256-word count per 4096-key tile
+        for n in (1, 4096, 12345, 1 << 28):
+            got = lib.gc_workspace_bytes(gc.OP_RADIX_SORT, n, dt)
+            table = -(-4 * 256 * -(-n // 4096) // 256) * 256
+            assert got == lib.gc_workspace_bytes(gc.OP_SPLIT_RADIX, n, gc.U32) + table, n
     assert lib.gc_workspace_bytes(gc.OP_RADIX_SORT, 12345, 7) == 0
-    assert lib.gc_tile_elements(gc.OP_RADIX_SORT) == lib.gc_tile_elements(gc.OP_SPLIT_RADIX)
+    assert lib.gc_tile_elements(gc.OP_RADIX_SORT) == 4096
 
 
 def test_binding_refuses_cpu_tensors(lib):
