@@ -168,9 +168,9 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
             typename Op::Loaded ld;
             if constexpr (Op::kPreload) {
                 if (full)
-                    op.template load<true>(pipe, ps, pbase, pstaged, n, ld);
+                    op.template load<true>(pipe, ps, pbase, pstaged, n, prev_agg, ld);
                 else
-                    op.template load<false>(pipe, ps, pbase, pstaged, n, ld);
+                    op.template load<false>(pipe, ps, pbase, pstaged, n, prev_agg, ld);
             }
             if constexpr (Op::kF32) {
                 float wh, wl_;
@@ -244,7 +244,8 @@ struct ScanOp {
     struct Loaded {};
 
     template <bool FULL, class P>
-    __device__ __forceinline__ void load(const P &, int, uint32_t, uint32_t, uint32_t, Loaded &) const {}
+    __device__ __forceinline__ void load(const P &, int, uint32_t, uint32_t, uint32_t, uint32_t,
+                                         Loaded &) const {}
 
     // The aggregate only: a plain sum, so it is published as early as possible.
     template <bool FULL, class P>
@@ -439,19 +440,44 @@ struct SelectOp {
         return rank_tile<TT, FULL>(pipe.buf(s), srcs[0], base, staged, n, pred, c.mask, c.base);
     }
 
+    // A tile with fewer survivors than this skips the in-place compaction:
+    // each thread stores its few survivors straight from the stage buffer.
+    static constexpr uint32_t kSparse = TT::kElems / 16;
+
     template <bool FULL, class P>
     __device__ __forceinline__ void load(const P &pipe, int s, uint32_t base, uint32_t staged,
-                                         uint32_t n, Loaded &ld) const
+                                         uint32_t n, uint32_t kept, Loaded &ld) const
     {
-        tile_vectors<TT, FULL>(pipe.buf(s), srcs[0], base, staged, n, ld.x);
+        if (kept >= kSparse) tile_vectors<TT, FULL>(pipe.buf(s), srcs[0], base, staged, n, ld.x);
     }
 
     template <bool FULL, class P>
-    __device__ __forceinline__ void finish(const P &pipe, int s, uint32_t tile, uint32_t, uint32_t,
-                                           uint32_t, uint32_t before, uint32_t kept, bool last,
-                                           const Carry &c, const Loaded &ld) const
+    __device__ __forceinline__ void finish(const P &pipe, int s, uint32_t tile, uint32_t base,
+                                           uint32_t staged, uint32_t n, uint32_t before,
+                                           uint32_t kept, bool last, const Carry &c,
+                                           const Loaded &ld) const
     {
         uint32_t *buf = pipe.buf(s);
+        if (kept < kSparse) {
+            // Survivor q of vector r goes to before + base[r] + (survivors of
+            // the vector before it); no shared-memory writes, so no barrier.
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                uint32_t m = c.mask[r];
+                uint32_t pos = before + c.base[r];
+                const uint32_t li = r * TT::kRowElems + 4 * threadIdx.x;
+                while (m != 0u) {
+                    const uint32_t q = uint32_t(__ffs(m) - 1);
+                    m &= m - 1u;
+                    const uint32_t x = (FULL || li + 4u <= staged) ? buf[li + q] : srcs[0][base + li + q];
+                    __stcs(out + pos, x);
+                    ++pos;
+                }
+            }
+            if (threadIdx.x == 0 && last) *count = before + kept;
+            (void)tile;
+            return;
+        }
         const uint32_t shift = VEC ? (before & 3u) : 0u;
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) {
@@ -537,7 +563,8 @@ struct PartitionOp {
     struct Loaded {};
 
     template <bool FULL, class P>
-    __device__ __forceinline__ void load(const P &, int, uint32_t, uint32_t, uint32_t, Loaded &) const {}
+    __device__ __forceinline__ void load(const P &, int, uint32_t, uint32_t, uint32_t, uint32_t,
+                                         Loaded &) const {}
 
     template <bool FULL, class P>
     __device__ __forceinline__ uint32_t reduce(const P &pipe, int s, uint32_t base, uint32_t staged,
