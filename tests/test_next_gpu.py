@@ -1,6 +1,7 @@
 """Parity of the widened entry points with the oracle, on the GPU through the C ABI:
-the inclusive scan and select-if / partition with parameterised predicates
-(every comparison in every dtype's order, and masked-bit tests).
+the inclusive scan, select-if / partition with parameterised predicates
+(every comparison in every dtype's order, and masked-bit tests), and the
+typed 8-bit-digit radix sort.
 
 Same bar as the core path: integer results bit-exact, float32 scans within
 1e-5 relative of the float64 oracle.
@@ -200,3 +201,20 @@ def test_radix_sort_float_at_scale(orc):
     ko, vo = gc.radix_sort(dev(x), dev(vals))
     assert np.array_equal(host(ko).view(np.uint32), wk.view(np.uint32))
     assert np.array_equal(host(vo), wv)
+
+
+def test_radix_sort_duplicates_and_uint32_at_scale(orc):
+    """2^25 int32 keys drawn from 1000 values (long runs of equal keys: stability
+    across tiles and passes), and 2^25 uint32 keys against the one-bit oracle."""
+    n = 1 << 25
+    rng = np.random.default_rng(4242)
+    x = (rng.integers(-500, 500, size=n)).astype(np.int32)
+    vals = np.arange(n, dtype=np.uint32)
+    wk, wv = orc.radix_sort(x, vals)
+    ko, vo = gc.radix_sort(dev(x), dev(vals))
+    assert np.array_equal(host(ko), wk)
+    assert np.array_equal(host(vo), wv)
+    ku, _ = synth.radix_keys(n, 77)
+    wk, wv = orc.split_radix(ku, vals)
+    ko, vo = gc.radix_sort(dev(ku), dev(vals))
+    assert np.array_equal(host(ko), wk) and np.array_equal(host(vo), wv)
