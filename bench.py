@@ -67,6 +67,8 @@ def parse_args(argv=None):
     p.add_argument("--n", type=int, default=1 << 28, help="elements per array (default 2^28)")
     p.add_argument("--cpu-sample", type=int, default=1 << 24,
                    help="elements per array in the timed CPU-oracle sample")
+    p.add_argument("--configs", action="store_true",
+                   help="instead of the step: one line per benchmark configuration at its own size")
     return p.parse_args(argv)
 
 
@@ -594,8 +596,134 @@ def run_reference(args):
     print(json.dumps(result), flush=True)
 
 
+# ---------------------------------------------------------------- per-configuration rows
+
+def run_configs(args):
+    """One JSON line per benchmark configuration at its own size: the GPU time
+    of the call through the C ABI (CUDA events on the launching stream, median
+    of 20 runs, L2 flushed by a 256 MiB write before every run, so the small
+    configurations are timed from HBM too) and the oracle's single-thread time
+    on the same input (median of 3 runs below 2^24 elements, else one run).
+    The flush reads, so that no dirty line of it is written back while the
+    timed call runs; inputs of 2^26 elements and more exceed L2 by
+    themselves and run without one."""
+    import torch
+
+    import oracle
+    from partition_pass_tile_gb300 import gc, synth
+
+    orc = oracle.default()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)  # 256 MiB, twice L2
+    peak, peak_kind = read_peaks()
+    gc.load()
+
+    def to_dev(a):
+        t = torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else a).to(dev)
+        return t.view(torch.uint32) if a.dtype == np.uint32 else t
+
+    def gpu_ms(fn, reps=20, n=0):
+        for _ in range(3):
+            fn()
+        times = []
+        for _ in range(reps):
+            if n < (1 << 26):
+                with torch.cuda.stream(stream):
+                    torch.max(flush)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            times.append((a, b))
+        torch.cuda.synchronize(dev)
+        return float(np.median([a.elapsed_time(b) for a, b in times]))
+
+    def cpu_ms(fn, n):
+        reps = 3 if n < (1 << 24) else 1
+        ts = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            fn()
+            ts.append((time.perf_counter() - t0) * 1e3)
+        return float(np.median(ts))
+
+    ws = gc.workspace(gc.OP_SPLIT_RADIX, 1 << 28, gc.F32, dev)
+    cnt = torch.zeros(4, dtype=torch.uint32, device=dev)
+
+    def row(config, n, op, ms, nbytes, oms, note=""):
+        r = {"config": config, "n": n, "op": op, "ms": round(ms, 4),
+             "gelem_s": round(n / ms / 1e6, 2), "alg_gbs": round(nbytes / ms / 1e6, 1),
+             "frac_of_peak": round(nbytes / ms / 1e6 / peak, 4), "peak": peak,
+             "peak_kind": peak_kind, "oracle_ms_1core": round(oms, 1)}
+        if note:
+            r["note"] = note
+        print(json.dumps(r), flush=True)
+
+    def select_row(config, x, pred, name):
+        n = x.shape[0]
+        xd = to_dev(x)
+        out = torch.empty_like(xd)
+        kept = int(np.count_nonzero(x != 0) if pred == "nonzero" else np.count_nonzero(x & 1))
+        ms = gpu_ms(lambda: gc.select_if(xd, pred, out=out, count=cnt[0:1], ws=ws, stream=stream), n=n)
+        code = oracle.NONZERO if pred == "nonzero" else oracle.ODD
+        row(config, n, name, ms, 4.0 * n + 4.0 * kept + 4, cpu_ms(lambda: orc.select_if(x, code), n))
+
+    def scan_row(config, x, name):
+        n = x.shape[0]
+        xd = to_dev(x)
+        out = torch.empty_like(xd)
+        tot = torch.empty(1, dtype=xd.dtype, device=dev)
+        ms = gpu_ms(lambda: gc.exclusive_scan(xd, out=out, total=tot, ws=ws, stream=stream), n=n)
+        row(config, n, name, ms, 8.0 * n, cpu_ms(lambda: orc.exclusive_scan(x), n))
+
+    select_row("1 remove zeros", synth.remove_zeros(), "nonzero", "select NONZERO")
+    scan_row("2 scan", synth.scan_mod8(), "exclusive scan int32 (i%8)+1")
+    scan_row("2 scan", synth.scan_unit_f32(), "exclusive scan float32 U[0,1)")
+    for n in (synth.SIZES["keep_odd"], synth.SIZES["keep_odd_literal"]):
+        x = synth.uniform_i32(n, synth.SEEDS["keep_odd"])
+        select_row("3 keep odd", x, "odd", "select ODD")
+        xd = to_dev(x)
+        out = torch.empty_like(xd)
+        ms = gpu_ms(lambda: gc.select_if_atomic(xd, "odd", out=out, count=cnt[1:2], ws=ws, stream=stream), n=n)
+        kept = int(np.count_nonzero(x & 1))
+        row("3 keep odd", n, "atomic comparator ODD (multiset)", ms, 4.0 * n + 4.0 * kept + 4,
+            cpu_ms(lambda: orc.select_if(x, oracle.ODD), n), "oracle: the ordered select")
+        del xd, out
+    n = synth.SIZES["partition"]
+    x = synth.uniform_i32(n, synth.SEEDS["partition"])
+    xd = to_dev(x)
+    out = torch.empty_like(xd)
+    ms = gpu_ms(lambda: gc.partition(xd, "even", out=out, count_true=cnt[2:3], ws=ws, stream=stream), n=n)
+    row("4 partition", n, "partition EVEN", ms, 8.0 * n, cpu_ms(lambda: orc.partition(x, oracle.EVEN), n),
+        "algorithmic 8 B/elem; the count pre-pass makes 12 B moved")
+    del xd, out
+    for p, seed in ((0.01, 41), (0.50, 42), (0.99, 43)):
+        select_row("4 sweep", synth.keep_fraction(n, p, seed), "nonzero", f"select NONZERO p={p}")
+    n = synth.SIZES["radix"]
+    keys, vals = synth.radix_keys(n, synth.SEEDS["radix"])
+    kd, vd = to_dev(keys), to_dev(vals)
+    ko, vo = torch.empty_like(kd), torch.empty_like(vd)
+    ms = gpu_ms(lambda: gc.split_radix(kd, vd, 0, 32, keys_out=ko, vals_out=vo, ws=ws, stream=stream), reps=5, n=n)
+    row("5 radix", n, "32 one-bit splits, uint32 keys + payload", ms, (16.0 * 32 + 4.0) * n,
+        cpu_ms(lambda: orc.split_radix(keys, vals), n))
+    ws_sort = gc.workspace(gc.OP_RADIX_SORT, n, gc.U32, dev)
+    ms = gpu_ms(lambda: gc.radix_sort(kd, vd, keys_out=ko, vals_out=vo, ws=ws_sort, stream=stream), reps=5, n=n)
+    row("5 radix", n, "gc_radix_sort (four 8-bit digit passes), same keys + payload", ms, 64.0 * n,
+        cpu_ms(lambda: orc.radix_sort(keys, vals), n), "algorithmic 64 B/key: keys and payloads once per pass")
+    del kd, vd, ko, vo, ws_sort
+    for n in (1 << 26, 1 << 28):
+        scan_row("roofline", synth.uniform_i32(n, synth.SEEDS["partition"]), "exclusive scan int32")
+        scan_row("roofline", synth.scan_unit_f32(n, synth.SEEDS["scan_f32"]), "exclusive scan float32")
+        select_row("roofline", synth.keep_fraction(n, 0.5, 42), "nonzero", "select NONZERO p=0.5")
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.configs:
+        run_configs(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -238,6 +238,30 @@ def test_one_workspace_serves_every_op(orc):
         assert gc.query_device_status(ws) == 0
 
 
+def test_workspace_reuse_small_sort_then_large_scan(orc):
+    """A workspace sized for the largest call, first used by small radix sorts
+    (whose ping-pong buffers and digit table sit where a much larger call's
+    status words go), then by a 64x larger scan and select: every call clears
+    its own status words, whatever the workspace held before."""
+    small, big = 100_003, 64 * 100_003
+    ws = gc.workspace(gc.OP_RADIX_SORT, big, gc.F32)
+    assert ws.numel() >= max(gc.workspace_bytes(op, big, gc.F32) for op in range(7))
+    keys, vals = synth.radix_keys(small, 9)
+    ko, vo = gc.split_radix(dev(keys), dev(vals), ws=ws)
+    assert np.array_equal(host(ko), orc.split_radix(keys, vals)[0])
+    kf = synth.scan_unit_f32(small, 9) - np.float32(0.5)
+    ko, _ = gc.radix_sort(dev(kf), None, ws=ws)
+    assert np.array_equal(host(ko).view(np.uint32), orc.radix_sort(kf)[0].view(np.uint32))
+    xf = synth.scan_unit_f32(big, 10)
+    out, _ = gc.exclusive_scan(dev(xf), ws=ws)
+    assert f32_within(host(out), orc.exclusive_scan(xf)[0])[0].size == 0
+    x = synth.uniform_i32(big, 10)
+    out, c = gc.select_if(dev(x), "odd", ws=ws)
+    w = orc.select_if(x, O.ODD)
+    assert int(host(c)[0]) == w.shape[0] and np.array_equal(host(out)[: w.shape[0]], w)
+    assert gc.query_device_status(ws) == 0
+
+
 def test_streams_and_empty_inputs():
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
