@@ -122,24 +122,45 @@ constexpr uint32_t kBulkMinRun = 512u;
 
 // Writes s[soff .. soff + len) to out[dst .. dst + len) when soff and dst
 // agree modulo 4 elements (16 bytes) and out is 16-byte aligned: the
-// aligned middle of the run goes out as one bulk copy issued by thread 0,
-// the ragged head and tail (at most 3 elements each) as plain stores by
-// threads 0-2 and 32-34.  The caller has made the run's shared-memory writes
-// visible to the async proxy (fence.proxy.async by every writer, then a
-// barrier) and commits thread 0's bulk group afterwards.
+// aligned middle of the run goes out as one bulk copy issued and committed
+// by lane 0 of warp `warp` (its own bulk group), the ragged head and tail
+// (at most 3 elements each) as plain stores by lanes 1-3 and 5-7 of that
+// warp.  The caller has made the run's shared-memory writes visible to the
+// async proxy (fence.proxy.async by every writer, then a barrier), and the
+// issuing lane waits for its group (bulk_wait_read_all) before the buffer is
+// used again.  Runs issued by different warps go out in parallel.
 template <int THREADS>
 __device__ __forceinline__ void store_run_bulk(uint32_t *__restrict__ out, uint32_t dst,
-                                               const uint32_t *s, uint32_t soff, uint32_t len)
+                                               const uint32_t *s, uint32_t soff, uint32_t len,
+                                               int warp)
 {
-    static_assert(THREADS >= 64, "head and tail threads");
-    if (len == 0u) return;
+    if (len == 0u || int(threadIdx.x >> 5) != warp) return;
     const uint32_t end = dst + len;
     const uint32_t a = min((dst + 3u) & ~3u, end);
     const uint32_t b = max(end & ~3u, a);
-    const uint32_t tid = threadIdx.x;
-    if (tid < a - dst) __stcs(out + dst + tid, s[soff + tid]);
-    if (tid >= 32u && tid - 32u < end - b) __stcs(out + b + (tid - 32u), s[soff + (b - dst) + (tid - 32u)]);
-    if (tid == 0u && b > a) bulk_store(out + a, s + soff + (a - dst), (b - a) * 4u);
+    const uint32_t lane = threadIdx.x & 31u;
+    if (lane >= 1u && lane - 1u < a - dst) __stcs(out + dst + (lane - 1u), s[soff + (lane - 1u)]);
+    if (lane >= 5u && lane - 5u < end - b)
+        __stcs(out + b + (lane - 5u), s[soff + (b - dst) + (lane - 5u)]);
+    if (lane == 0u && b > a) {
+        bulk_store(out + a, s + soff + (a - dst), (b - a) * 4u);
+        bulk_commit();
+    }
+}
+
+// Warps whose lane 0 may issue bulk stores of a tile's runs.
+constexpr int kBulkIssuers = 4;
+
+// Every issuing lane: until its bulk stores have read their shared source.
+__device__ __forceinline__ void bulk_issuers_wait_read()
+{
+    if ((threadIdx.x & 31u) == 0u && (threadIdx.x >> 5) < unsigned(kBulkIssuers)) bulk_wait_read_all();
+}
+
+// Every issuing lane: until its bulk stores are complete.
+__device__ __forceinline__ void bulk_issuers_wait_all()
+{
+    if ((threadIdx.x & 31u) == 0u && (threadIdx.x >> 5) < unsigned(kBulkIssuers)) bulk_wait_all();
 }
 
 // Waits for a stage's phase.  The wait is bounded: past timeout_ns of device

@@ -120,6 +120,7 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
                                              uint32_t num_tiles, uint8_t *ws, uint64_t timeout_ns)
 {
     static_assert(STAGES >= 3, "the tile being reduced, the tile being finished, one in flight");
+    static_assert(THREADS >= 32 * kBulkIssuers, "a warp per bulk-store issuer");
     using P = typename Op::template PipeT<STAGES>;
     constexpr uint32_t TE = Op::kTileElems;
     constexpr int W = THREADS / 32;
@@ -195,17 +196,15 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
                 else
                     op.template finish<false>(pipe, ps, prev, pbase, pstaged, n, prefix, prev_agg, last, prv, ld);
             }
-            __syncthreads();  // the previous tile's stage is free again
-            if (tid == 0) {
-                bulk_wait_read_all();  // ... once its bulk stores have read it
-                pipe.refill(ps, op.srcs, prev, TE, n, num_tiles);
-            }
+            bulk_issuers_wait_read();  // the stage's bulk stores have read it ...
+            __syncthreads();           // ... and every thread is done with it
+            if (tid == 0) pipe.refill(ps, op.srcs, prev, TE, n, num_tiles);
         }
         if (!have) break;
         prev_agg = agg;
         prv = cur;
     }
-    if (tid == 0) bulk_wait_all();  // shared memory stays until the stores are done
+    bulk_issuers_wait_all();  // shared memory stays until the stores are done
 }
 
 // Grid limit of pipeline_run: the window of a tile must fit kWinPerThread
@@ -489,8 +488,7 @@ struct SelectOp {
         if (VEC && kept >= kBulkMinRun) {
             fence_proxy_async_smem();
             __syncthreads();
-            store_run_bulk<THREADS>(out, before, buf, shift, kept);
-            if (threadIdx.x == 0) bulk_commit();
+            store_run_bulk<THREADS>(out, before, buf, shift, kept, 0);
         } else {
             __syncthreads();
             store_run<THREADS, VEC>(out, before, buf, shift, kept);
@@ -636,13 +634,12 @@ struct PartitionOp {
             // The runs leave by bulk copies from the stage buffer(s).
             fence_proxy_async_smem();
             __syncthreads();
-            store_run_bulk<THREADS>(keys_out, dst_kept, kbuf, sh_kept, kept_len);
-            store_run_bulk<THREADS>(keys_out, dst_rej, kbuf, sh_rej, rejected);
+            store_run_bulk<THREADS>(keys_out, dst_kept, kbuf, sh_kept, kept_len, 0);
+            store_run_bulk<THREADS>(keys_out, dst_rej, kbuf, sh_rej, rejected, 1);
             if (VALS) {
-                store_run_bulk<THREADS>(vals_out, dst_kept, vbuf, sh_kept, kept_len);
-                store_run_bulk<THREADS>(vals_out, dst_rej, vbuf, sh_rej, rejected);
+                store_run_bulk<THREADS>(vals_out, dst_kept, vbuf, sh_kept, kept_len, 2);
+                store_run_bulk<THREADS>(vals_out, dst_rej, vbuf, sh_rej, rejected, 3);
             }
-            if (tid == 0) bulk_commit();
         } else {
             __syncthreads();
             store_run<THREADS, VEC>(keys_out, dst_kept, kbuf, sh_kept, kept_len);
