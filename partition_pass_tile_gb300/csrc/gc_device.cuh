@@ -834,8 +834,16 @@ __device__ __forceinline__ V block_sum_all(V v, V *s_red)
 // (in s_chunk, chunk c = row * WARPS + warp) by itself and keeps the offsets
 // of its own chunks, one per row, plus the tile total: one barrier (before
 // the call) serves both the tile's reduction and its ranking.
-template <class TT, class V>
-__device__ __forceinline__ void chunk_offsets(const V *s_chunk, V (&off)[TT::kRows], V &total)
+struct NoTotalHook {
+    template <class V>
+    __device__ __forceinline__ void operator()(V) const {}
+};
+
+// on_total(total) runs as soon as the tile total is known, before the
+// per-row offsets (a caller publishes it without waiting for them).
+template <class TT, class V, class OnTotal = NoTotalHook>
+__device__ __forceinline__ void chunk_offsets(const V *s_chunk, V (&off)[TT::kRows], V &total,
+                                              const OnTotal &on_total = OnTotal{})
 {
     constexpr int K = TT::kChunksPerLane;
     constexpr bool kShort = TT::kChunks < 32;
@@ -854,6 +862,7 @@ __device__ __forceinline__ void chunk_offsets(const V *s_chunk, V (&off)[TT::kRo
         if (lane >= o) incl += y;
     }
     total = __shfl_sync(kFullMask, incl, 31);
+    on_total(total);
     V e[K];
     e[0] = __shfl_up_sync(kFullMask, incl, 1);
     if (lane == 0) e[0] = V(0);

@@ -153,11 +153,14 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
             mbar_wait(pipe.bar(s), (k / STAGES) & 1u, ws, timeout_ns);
             const uint32_t base = tile * TE;
             const uint32_t staged = staged_elems(tile, TE, n);
+            // Publishes t's aggregate: every op calls it once, as soon as it is known.
+            auto publish = [&](uint32_t bits) {
+                if (tid == 0) publish_aggregate(status, tile, bits);
+            };
             if (staged == TE)
-                agg = op.template reduce<true>(pipe, s, base, staged, n, cur);
+                agg = op.template reduce<true>(pipe, s, base, staged, n, cur, publish);
             else
-                agg = op.template reduce<false>(pipe, s, base, staged, n, cur);
-            if (tid == 0) publish_aggregate(status, tile, agg);
+                agg = op.template reduce<false>(pipe, s, base, staged, n, cur, publish);
         }
 
         if (have_prev) {
@@ -247,9 +250,9 @@ struct ScanOp {
                                          Loaded &) const {}
 
     // The aggregate only: a plain sum, so it is published as early as possible.
-    template <bool FULL, class P>
+    template <bool FULL, class P, class Publish>
     __device__ __forceinline__ uint32_t reduce(const P &pipe, int s, uint32_t base, uint32_t staged,
-                                               uint32_t n, Carry &) const
+                                               uint32_t n, Carry &, const Publish &publish) const
     {
         __shared__ uint32_t s_red[TT::kWarps];
         const int tid = threadIdx.x;
@@ -262,7 +265,9 @@ struct ScanOp {
                 a += (__uint_as_float(x[0]) + __uint_as_float(x[1])) +
                      (__uint_as_float(x[2]) + __uint_as_float(x[3]));
             }
-            return __float_as_uint(block_sum_all<THREADS>(a, reinterpret_cast<float *>(s_red)));
+            const uint32_t agg = __float_as_uint(block_sum_all<THREADS>(a, reinterpret_cast<float *>(s_red)));
+            publish(agg);
+            return agg;
         } else {
             uint32_t a = 0u;
 #pragma unroll
@@ -271,7 +276,9 @@ struct ScanOp {
                 stage_load4<FULL>(pipe.buf(s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x);
                 a += x[0] + x[1] + x[2] + x[3];
             }
-            return block_sum_all<THREADS>(a, s_red);
+            const uint32_t agg = block_sum_all<THREADS>(a, s_red);
+            publish(agg);
+            return agg;
         }
     }
 
@@ -385,11 +392,11 @@ __device__ __forceinline__ void tile_masks(const uint32_t *sbuf, const uint32_t 
 
 // Reduction of a predicate tile: masks, in-tile ranks and the keep count.
 // base[r] = survivors of the tile before this thread's vector r.
-template <class TT, bool FULL, class Pred>
+template <class TT, bool FULL, class Pred, class OnTotal>
 __device__ __forceinline__ uint32_t rank_tile(const uint32_t *sbuf, const uint32_t *gin,
                                               uint32_t base, uint32_t staged, uint32_t n,
                                               const Pred &pred, uint32_t (&mask)[TT::kRows],
-                                              uint32_t (&rbase)[TT::kRows])
+                                              uint32_t (&rbase)[TT::kRows], const OnTotal &on_total)
 {
     __shared__ uint32_t s_chunk[TT::kChunks];
     tile_masks<TT, FULL>(sbuf, gin, base, staged, n, pred, mask);
@@ -397,7 +404,7 @@ __device__ __forceinline__ uint32_t rank_tile(const uint32_t *sbuf, const uint32
     rank_masks<TT>(mask, lane_excl, s_chunk);
     __syncthreads();
     uint32_t off[TT::kRows], kept;
-    chunk_offsets<TT>(s_chunk, off, kept);
+    chunk_offsets<TT>(s_chunk, off, kept, on_total);
 #pragma unroll
     for (int r = 0; r < TT::kRows; ++r) rbase[r] = off[r] + lane_excl[r];
     return kept;
@@ -432,11 +439,12 @@ struct SelectOp {
         uint32_t x[ROWS][4];
     };
 
-    template <bool FULL, class P>
+    template <bool FULL, class P, class Publish>
     __device__ __forceinline__ uint32_t reduce(const P &pipe, int s, uint32_t base, uint32_t staged,
-                                               uint32_t n, Carry &c) const
+                                               uint32_t n, Carry &c, const Publish &publish) const
     {
-        return rank_tile<TT, FULL>(pipe.buf(s), srcs[0], base, staged, n, pred, c.mask, c.base);
+        // The count goes out before the per-row ranks are derived.
+        return rank_tile<TT, FULL>(pipe.buf(s), srcs[0], base, staged, n, pred, c.mask, c.base, publish);
     }
 
     // A tile with fewer survivors than this skips the in-place compaction:
@@ -564,12 +572,14 @@ struct PartitionOp {
     __device__ __forceinline__ void load(const P &, int, uint32_t, uint32_t, uint32_t, uint32_t,
                                          Loaded &) const {}
 
-    template <bool FULL, class P>
+    template <bool FULL, class P, class Publish>
     __device__ __forceinline__ uint32_t reduce(const P &pipe, int s, uint32_t base, uint32_t staged,
-                                               uint32_t n, Carry &c) const
+                                               uint32_t n, Carry &c, const Publish &publish) const
     {
         __shared__ uint32_t s_red[TT::kWarps];
-        return tile_count<TT, FULL>(pipe.buf(s), srcs[0], base, staged, n, pred, s_red, c.mask);
+        const uint32_t agg = tile_count<TT, FULL>(pipe.buf(s), srcs[0], base, staged, n, pred, s_red, c.mask);
+        publish(agg);
+        return agg;
     }
 
     template <bool FULL, class P>
