@@ -17,9 +17,9 @@
 //      per-tile offsets.
 //   3. digit_scatter_kernel: every tile ranks its keys stably within the
 //      tile (warp by warp, 32 keys at a time: peers found by one ballot per
-//      digit bit, per-warp digit counters in shared memory), sorts them by digit in shared
-//      memory, and writes each digit's run to A[d * T + t] onwards, so
-//      consecutive threads store consecutive addresses.
+//      digit bit, per-warp digit counters in shared memory), sorts them by
+//      digit in shared memory, and writes each digit's run to A[d * T + t]
+//      onwards, so consecutive threads store consecutive addresses.
 //
 // Keys of int32 and float32 are sorted by the order-preserving key of
 // PredKeyBitClear, x ^ (signfill(x) & neg) ^ flip: its digits are computed
@@ -40,7 +40,7 @@ constexpr uint32_t kSegment = 32u * kDigitItems;  // keys per warp, in order
 static_assert(kDigitThreads == int(kDigits), "one thread per digit");
 static_assert(gch::kDigitTile == kDigitThreads * kDigitItems, "tile size");
 
-// Digit of x at `shift` under the order-preserving key map; 256 for padding.
+// Digit of x at `shift` under the order-preserving key map.
 struct DigitOf {
     uint32_t neg, flip, shift;
     __device__ __forceinline__ uint32_t operator()(uint32_t x) const
