@@ -31,6 +31,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -56,6 +57,7 @@ OPS = ["scan_i32", "scan_f32", "select_p01", "select_p50", "select_p99", "partit
 LAUNCHES_PER_OP = {"scan_i32": 1, "scan_f32": 1, "select_p01": 1, "select_p50": 1,
                    "select_p99": 1, "partition": 2, "radix32": 33, "atomic_p50": 1}
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, NVIDIA's nominal figure: a secondary denominator
 
 
 def parse_args(argv=None):
@@ -265,17 +267,51 @@ def oracle_step(orc, h: dict, n: int) -> dict:
     return t
 
 
+def host_cpu() -> dict:
+    """The host's core count and CPU model, for the CPU-baseline record."""
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware") and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    if key == "model name":
+                        break
+    except OSError:
+        pass
+    return {"nproc": os.cpu_count(), "cpu": model or platform.machine()}
+
+
+class OneCore:
+    """Pins the calling process to one core (the first it may use) while the
+    single-threaded oracle is timed, then restores the affinity."""
+
+    def __enter__(self):
+        self.saved = None
+        if hasattr(os, "sched_getaffinity"):
+            self.saved = os.sched_getaffinity(0)
+            os.sched_setaffinity(0, {min(self.saved)})
+        return self
+
+    def __exit__(self, *exc):
+        if self.saved is not None:
+            os.sched_setaffinity(0, self.saved)
+        return False
+
+
 def cpu_baseline(h: dict, sample: int) -> dict:
     import oracle
     oracle.build()
     orc = oracle.default()
     sample = min(sample, h["x"].shape[0])
-    t = oracle_step(orc, h, sample)
+    with OneCore():
+        t = oracle_step(orc, h, sample)
     total = sum(t.values())
     return {"value": len(OPS) * sample / total / 1e9, "unit": "Gelem/s", "cores": 1,
-            "kind": "oracle",
+            "kind": "oracle", **host_cpu(),
             "sample": f"first {sample} elements of every input array, one pass of all "
-                      f"{len(OPS)} operations, single-threaded C, {total:.2f} s",
+                      f"{len(OPS)} operations, single-threaded C pinned to one core, {total:.2f} s",
             "ms_per_op": {k: round(v * 1e3, 3) for k, v in t.items()}}
 
 
@@ -540,6 +576,8 @@ def run_gc(args):
                                      "scaled by n/2^26 (profiles/dram_traffic.json); null if "
                                      "the kernels changed since",
                      "alg_bytes_per_launch": split_bytes,
+                     "peak_nominal": NOMINAL_HBM_GBS,
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                      "duration_note": "radix32 call time / 32: includes the histogram pass "
                                       "and each split's status-word clear"},
         "clocks": clocks.summary(),
@@ -571,12 +609,13 @@ def run_reference(args):
     orc = oracle.default()
     sample = min(args.cpu_sample >> 2, args.n)
     h = host_inputs(sample, 0)
-    for _ in range(max(args.warmup, 0)):
-        oracle_step(orc, h, sample)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle_step(orc, h, sample)
-    sec = (time.perf_counter() - t0) / max(args.steps, 1)
+    with OneCore():
+        for _ in range(max(args.warmup, 0)):
+            oracle_step(orc, h, sample)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle_step(orc, h, sample)
+        sec = (time.perf_counter() - t0) / max(args.steps, 1)
     value = len(OPS) * sample / sec / 1e9
     result = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "Gelem/s",
@@ -586,10 +625,10 @@ def run_reference(args):
         "config": {"workload": workload_name(args.n), "n": args.n, "sample_n": sample,
                    "ops_per_step": OPS, "parallelism": "host CPU, one core"},
         "cpu_baseline": {"value": round(value, 4), "unit": "Gelem/s", "kind": "oracle",
-                         "cores": 1,
+                         "cores": 1, **host_cpu(),
                          "sample": f"each step: the first {sample} elements of every input "
                                    f"array of the n={args.n} workload, all {len(OPS)} "
-                                   "operations, single-threaded C oracle"},
+                                   "operations, single-threaded C oracle pinned to one core"},
         "e2e": {"value": round(value, 4), "unit": "Gelem/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -638,25 +677,29 @@ def run_configs(args):
             b.record(stream)
             times.append((a, b))
         torch.cuda.synchronize(dev)
-        return float(np.median([a.elapsed_time(b) for a, b in times]))
+        ts = [a.elapsed_time(b) for a, b in times]
+        return float(np.median(ts)), float(np.min(ts))
 
     def cpu_ms(fn, n):
         reps = 3 if n < (1 << 24) else 1
         ts = []
-        for _ in range(reps):
-            t0 = time.perf_counter()
-            fn()
-            ts.append((time.perf_counter() - t0) * 1e3)
+        with OneCore():
+            for _ in range(reps):
+                t0 = time.perf_counter()
+                fn()
+                ts.append((time.perf_counter() - t0) * 1e3)
         return float(np.median(ts))
 
     ws = gc.workspace(gc.OP_SPLIT_RADIX, 1 << 28, gc.F32, dev)
     cnt = torch.zeros(4, dtype=torch.uint32, device=dev)
 
-    def row(config, n, op, ms, nbytes, oms, note=""):
-        r = {"config": config, "n": n, "op": op, "ms": round(ms, 4),
+    def row(config, n, op, t, nbytes, oms, note=""):
+        ms, best = t
+        r = {"config": config, "n": n, "op": op, "ms": round(ms, 4), "ms_best": round(best, 4),
              "gelem_s": round(n / ms / 1e6, 2), "alg_gbs": round(nbytes / ms / 1e6, 1),
              "frac_of_peak": round(nbytes / ms / 1e6 / peak, 4), "peak": peak,
-             "peak_kind": peak_kind, "oracle_ms_1core": round(oms, 1)}
+             "peak_kind": peak_kind, "frac_of_nominal": round(nbytes / ms / 1e6 / NOMINAL_HBM_GBS, 4),
+             "oracle_ms_1core": round(oms, 1), **host_cpu()}
         if note:
             r["note"] = note
         print(json.dumps(r), flush=True)
