@@ -280,6 +280,9 @@ def host_cpu() -> dict:
                         break
     except OSError:
         pass
+    arm_parts = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1", "0xd0c": "Arm Neoverse N1",
+                 "0xd8e": "Arm Neoverse N3", "0xd84": "Arm Neoverse V3"}
+    model = arm_parts.get(model.lower(), model)
     return {"nproc": os.cpu_count(), "cpu": model or platform.machine()}
 
 
