@@ -145,13 +145,11 @@ __device__ __forceinline__ void scatter_tile(const uint32_t *__restrict__ kin,
 
     // Warp w owns keys [w * kSegment, (w + 1) * kSegment) of the tile, taken
     // 32 at a time in order: key j of the warp's step s is lane j.
-    uint32_t k[kDigitItems], v[VALS ? kDigitItems : 1];
+    uint32_t k[kDigitItems];
 #pragma unroll
     for (int s = 0; s < kDigitItems; ++s) {
         const uint32_t li = uint32_t(warp) * kSegment + uint32_t(s) * 32u + uint32_t(lane);
-        const bool ok = FULL || li < valid;
-        k[s] = ok ? kin[base + li] : 0u;
-        if (VALS) v[VALS ? s : 0] = ok ? vin[base + li] : 0u;
+        k[s] = (FULL || li < valid) ? kin[base + li] : 0u;
     }
     // Digits: packed four to a word in a full tile; whole words, with the
     // padding value kDigits past the end, in the ragged one.
@@ -169,33 +167,41 @@ __device__ __forceinline__ void scatter_tile(const uint32_t *__restrict__ kin,
     auto digit = [&](int s) -> uint32_t {
         return FULL ? (dg[s >> 2] >> (8 * (s & 3))) & (kDigits - 1u) : dg[s];
     };
-    // Peers with the same digit in each step: independent of one another.
-    uint32_t peers[kDigitItems];
-#pragma unroll
-    for (int s = 0; s < kDigitItems; ++s)
-        peers[s] = digit_peers<FULL ? kDigitBits : kDigitBits + 1>(digit(s));
     __syncthreads();  // the counters are cleared
 
-    // Stable rank within the warp's segment: the step's leader for each digit
+    // Stable rank within the warp's segment: the peers of a key are the
+    // lanes of its step with the same digit; the step's leader for each digit
     // (its lowest lane) adds the group to the warp's counter and keeps the old
-    // value for its peers.  Only this load-store chain runs step by step.
+    // value for its peers.  Ranks (below kSegment) are kept two to a word.
     const uint32_t lt_mask = (1u << lane) - 1u;
-    uint32_t rank[kDigitItems];
+    uint32_t rank2[kDigitItems / 2];
 #pragma unroll
     for (int s = 0; s < kDigitItems; ++s) {
         const uint32_t ds = digit(s);
+        const uint32_t peers = digit_peers<FULL ? kDigitBits : kDigitBits + 1>(ds);
         uint32_t before = 0u;
-        if ((peers[s] & lt_mask) == 0u && (FULL || ds < kDigits)) {
+        if ((peers & lt_mask) == 0u && (FULL || ds < kDigits)) {
             before = sm.cnt[warp][ds];
-            sm.cnt[warp][ds] = before + uint32_t(__popc(peers[s]));
+            sm.cnt[warp][ds] = before + uint32_t(__popc(peers));
         }
         // The next step's leader for this digit may be another lane: order
         // this step's counter writes before its reads.
         __syncwarp();
-        rank[s] = __shfl_sync(kFullMask, before, __ffs(peers[s]) - 1) +
-                  uint32_t(__popc(peers[s] & lt_mask));
+        const uint32_t r = __shfl_sync(kFullMask, before, __ffs(peers) - 1) + uint32_t(__popc(peers & lt_mask));
+        if ((s & 1) == 0) rank2[s >> 1] = r;
+        else rank2[s >> 1] |= r << 16;
     }
     __syncthreads();
+    // The payloads are read only now, when the ranking no longer needs the
+    // registers; their latency overlaps the scans below.
+    uint32_t v[VALS ? kDigitItems : 1];
+    if (VALS) {
+#pragma unroll
+        for (int s = 0; s < kDigitItems; ++s) {
+            const uint32_t li = uint32_t(warp) * kSegment + uint32_t(s) * 32u + uint32_t(lane);
+            v[VALS ? s : 0] = (FULL || li < valid) ? vin[base + li] : 0u;
+        }
+    }
 
     // Per digit (thread tid = digit): exclusive scan over the warps, then over
     // the digits for the tile-local run starts.
@@ -225,7 +231,7 @@ __device__ __forceinline__ void scatter_tile(const uint32_t *__restrict__ kin,
     for (int s = 0; s < kDigitItems; ++s) {
         const uint32_t ds = digit(s);
         if (FULL || ds < kDigits) {
-            const uint32_t pos = sm.start[ds] + sm.cnt[warp][ds] + rank[s];
+            const uint32_t pos = sm.start[ds] + sm.cnt[warp][ds] + ((rank2[s >> 1] >> (16 * (s & 1))) & 0xffffu);
             sm.keys[pos] = k[s];
             if (VALS) s_vals[pos] = v[VALS ? s : 0];
         }
@@ -253,8 +259,14 @@ __device__ __forceinline__ void scatter_tile(const uint32_t *__restrict__ kin,
 
 // Pass step 3: stable scatter of one tile by digit.  offsets[d * T + t] is
 // where tile t's run of digit d starts in the output.
+// Resident CTAs per SM the scatter is compiled for (registers: 4 -> 64): the
+// kernel is latency-bound, and 4 CTAs per SM beat 2, 3 and 5.
+#ifndef GC_DIGIT_SCATTER_MIN_BLOCKS
+#define GC_DIGIT_SCATTER_MIN_BLOCKS 4
+#endif
+
 template <bool VALS>
-__global__ void __launch_bounds__(kDigitThreads, 3)
+__global__ void __launch_bounds__(kDigitThreads, GC_DIGIT_SCATTER_MIN_BLOCKS)
 digit_scatter_kernel(const uint32_t *__restrict__ kin, const uint32_t *__restrict__ vin,
                      uint32_t *__restrict__ kout, uint32_t *__restrict__ vout, uint32_t n,
                      DigitOf dig, const uint32_t *__restrict__ offsets, uint32_t tiles,
