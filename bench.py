@@ -160,10 +160,18 @@ def read_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# Sources that build the kernels profiles/dram_traffic.json records (the
+# persistent scan, select and partition kernels and their launchers); the
+# digit sort and the workspace-free entry point build none of them.
+TRAFFIC_SOURCES_EXCLUDED = {"radix.cu", "noalloc.cu"}
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "partition_pass_tile_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
+        if name in TRAFFIC_SOURCES_EXCLUDED:
+            continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
