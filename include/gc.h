@@ -27,8 +27,11 @@
  *                        built on scan); each split is gc_partition with the
  *                        predicate "bit b is 0".
  *   gc_radix_sort        full-width stable ascending sort of int32, uint32 or
- *                        float32 keys (IEEE 754 totalOrder), the same one-bit
- *                        splits over an order-preserving key.  The radix
+ *                        float32 keys (IEEE 754 totalOrder) by 8-bit digits,
+ *                        four passes: the one-bit split generalised to a
+ *                        256-way split addressed by a scan of per-tile digit
+ *                        counts ("CIS 565 Project 2", radix sort built on
+ *                        scan), over an order-preserving key.  The radix
  *                        passage sorts unsigned keys only; the key map is
  *                        the standard sign-flip reading of "sort by the
  *                        value" for the other two dtypes.
@@ -244,13 +247,17 @@ gc_status gc_split_radix(const uint32_t *d_keys_in, const uint32_t *d_vals_in,
  * Stable ascending radix sort of n keys of dtype, payloads carried: int32 in
  * signed order, uint32 in unsigned order, float32 in IEEE 754 totalOrder
  * (-NaN < -inf < negatives < -0 < +0 < positives < +inf < +NaN; NaNs by
- * payload bits, as patterns).  Equal keys keep their input order.  Bit b of
- * the order-preserving key k(x) = x ^ (signfill(x) & neg) ^ flip (int32: neg
- * 0, flip 2^31; float32: neg 2^31 - 1, flip 2^31; uint32: both 0) drives
- * split b, b = 0..31; the keys are moved as they are, never rewritten, so
- * d_keys_out holds the input's own bit patterns.  Same array rules, aliasing
- * and workspace layout as gc_split_radix (workspace:
- * gc_workspace_bytes(GC_OP_RADIX_SORT, n, dtype)).  Keys are d_keys_in /
+ * payload bits, as patterns).  Equal keys keep their input order.  The
+ * sort runs four stable passes over the 8-bit digits, lowest first, of the
+ * order-preserving key k(x) = x ^ (signfill(x) & neg) ^ flip (int32: neg 0,
+ * flip 2^31; float32: neg 2^31 - 1, flip 2^31; uint32: both 0); each pass
+ * is three launches (digit counts per 4096-key tile, one scan of the
+ * counts, the scatter).  The keys are moved as they are, never rewritten,
+ * so d_keys_out holds the input's own bit patterns.  The same array and
+ * aliasing rules as gc_split_radix: keys and payloads both or keys alone,
+ * an input may equal its output, no other overlap.  The workspace,
+ * gc_workspace_bytes(GC_OP_RADIX_SORT, n, dtype), holds the ping-pong
+ * buffers and a table of 256 counts per tile.  Keys are d_keys_in /
  * d_keys_out as void * to any of the three dtypes, 4-byte aligned.
  */
 gc_status gc_radix_sort(const void *d_keys_in, const uint32_t *d_vals_in,
