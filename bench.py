@@ -651,9 +651,10 @@ def run_reference(args):
 def run_configs(args):
     """One JSON line per benchmark configuration at its own size: the GPU time
     of the call through the C ABI (CUDA events on the launching stream, median
-    of 20 runs, L2 flushed by a 256 MiB write before every run, so the small
-    configurations are timed from HBM too) and the oracle's single-thread time
-    on the same input (median of 3 runs below 2^24 elements, else one run).
+    of 20 runs, L2 flushed by a 256 MiB read before every run, so the small
+    configurations are timed from HBM too), the same calls replayed from a
+    CUDA graph, and the oracle's single-thread time on the same input (median
+    of 3 runs below 2^24 elements, else one run).
     The flush reads, so that no dirty line of it is written back while the
     timed call runs; inputs of 2^26 elements and more exceed L2 by
     themselves and run without one."""
@@ -675,21 +676,33 @@ def run_configs(args):
         return t.view(torch.uint32) if a.dtype == np.uint32 else t
 
     def gpu_ms(fn, reps=20, n=0):
+        """Median and best time of fn(), and the median of the same calls
+        captured once in a CUDA graph and replayed (launch gaps shrink)."""
         for _ in range(3):
             fn()
-        times = []
-        for _ in range(reps):
-            if n < (1 << 26):
-                with torch.cuda.stream(stream):
-                    torch.max(flush)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
             fn()
-            b.record(stream)
-            times.append((a, b))
         torch.cuda.synchronize(dev)
-        ts = [a.elapsed_time(b) for a, b in times]
-        return float(np.median(ts)), float(np.min(ts))
+        out = []
+        for run in (fn, graph.replay):
+            times = []
+            for _ in range(reps):
+                if n < (1 << 26):
+                    with torch.cuda.stream(stream):
+                        torch.max(flush)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                if run is fn:
+                    fn()
+                else:
+                    with torch.cuda.stream(stream):
+                        graph.replay()
+                b.record(stream)
+                times.append((a, b))
+            torch.cuda.synchronize(dev)
+            out.append([a.elapsed_time(b) for a, b in times])
+        return float(np.median(out[0])), float(np.min(out[0])), float(np.median(out[1]))
 
     def cpu_ms(fn, n):
         reps = 3 if n < (1 << 24) else 1
@@ -705,8 +718,9 @@ def run_configs(args):
     cnt = torch.zeros(4, dtype=torch.uint32, device=dev)
 
     def row(config, n, op, t, nbytes, oms, note=""):
-        ms, best = t
+        ms, best, graphed = t
         r = {"config": config, "n": n, "op": op, "ms": round(ms, 4), "ms_best": round(best, 4),
+             "ms_graph": round(graphed, 4),
              "gelem_s": round(n / ms / 1e6, 2), "alg_gbs": round(nbytes / ms / 1e6, 1),
              "frac_of_peak": round(nbytes / ms / 1e6 / peak, 4), "peak": peak,
              "peak_kind": peak_kind, "frac_of_nominal": round(nbytes / ms / 1e6 / NOMINAL_HBM_GBS, 4),
