@@ -136,6 +136,13 @@ inline size_t digit_table_bytes(size_t n) { return align_up(4 * 256 * ceil_div(n
 struct LaunchOpts {
     uint64_t timeout_ns = 1000000000ull;  // a look-back wait gives up after this long
     bool skip_first_tile = false;        // test hook: no CTA ever takes tile 0
+    // Status words of a persistent kernel.  By default a call clears its own
+    // (region 0) with a memset first.  A caller that runs many passes in a
+    // row (the radix split) may instead give each pass the region starting at
+    // word status_region, already clear, and have it clear clear_words words
+    // from clear_region on for the next pass: then no memset runs.
+    bool reset_status = true;
+    uint32_t status_region = 0, clear_region = 0, clear_words = 0;
 };
 
 // Clears the tile counter and `tiles` status words; then the kernel of the

@@ -17,10 +17,11 @@ namespace gcd {
 
 template <int THREADS, int STAGES, class Op>
 __global__ void GC_PIPE_BOUNDS(THREADS)
-pipeline_kernel(Op op, uint32_t n, uint32_t num_tiles, uint8_t *ws, uint64_t timeout_ns)
+pipeline_kernel(Op op, uint32_t n, uint32_t num_tiles, uint8_t *ws, uint64_t timeout_ns,
+                StatusPlan plan)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    pipeline_run<THREADS, STAGES>(op, smem, n, num_tiles, ws, timeout_ns);
+    pipeline_run<THREADS, STAGES>(op, smem, n, num_tiles, ws, timeout_ns, plan);
 }
 
 // Clears this call's tile status words and launches the cooperative
@@ -29,18 +30,23 @@ pipeline_kernel(Op op, uint32_t n, uint32_t num_tiles, uint8_t *ws, uint64_t tim
 // grid right now) lets the caller fall back to a one-tile-per-CTA kernel.
 template <int THREADS, int STAGES, class Op>
 cudaError_t launch_pipeline(const Op &op, uint32_t n, uint8_t *ws, cudaStream_t s,
-                            uint64_t timeout_ns)
+                            const gch::LaunchOpts &o)
 {
     uint32_t tiles = uint32_t(gch::ceil_div(n, Op::kTileElems));
-    cudaError_t e = gch::reset_tiles(ws, tiles, s, false);
-    if (e != cudaSuccess) return e;
+    if (o.reset_status) {
+        const cudaError_t e = gch::reset_tiles(ws, tiles, s, false);
+        if (e != cudaSuccess) return e;
+    }
+    StatusPlan plan{o.reset_status ? 0u : o.status_region, o.clear_region,
+                    o.reset_status ? 0u : o.clear_words};
+    uint64_t timeout_ns = o.timeout_ns;
     auto kernel = pipeline_kernel<THREADS, STAGES, Op>;
     constexpr uint32_t smem = Op::template PipeT<STAGES>::kBytes;
     int grid = gch::persistent_grid(reinterpret_cast<const void *>(kernel), THREADS, smem, tiles);
     if (grid <= 0) return cudaErrorInvalidConfiguration;
     grid = std::min(grid, pipeline_max_grid<THREADS>());
     Op op_copy = op;
-    void *args[] = {&op_copy, &n, &tiles, &ws, &timeout_ns};
+    void *args[] = {&op_copy, &n, &tiles, &ws, &timeout_ns, &plan};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kernel), dim3(grid),
                                        dim3(THREADS), args, smem, s);
 }

@@ -115,9 +115,16 @@ __device__ __forceinline__ void window_finish_ff(const uint64_t *status, uint32_
 //     before the writes op.finish may make into it);
 //   op.finish(p): outputs from the carried offsets;
 //   a barrier, then p's stage is re-armed.
+// Where a persistent call's status words are (word offset from the status
+// area) and which words, already unused, it clears for the call after it.
+struct StatusPlan {
+    uint32_t region, clear_region, clear_words;
+};
+
 template <int THREADS, int STAGES, class Op>
 __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32_t n,
-                                             uint32_t num_tiles, uint8_t *ws, uint64_t timeout_ns)
+                                             uint32_t num_tiles, uint8_t *ws, uint64_t timeout_ns,
+                                             const StatusPlan &plan)
 {
     static_assert(STAGES >= 3, "the tile being reduced, the tile being finished, one in flight");
     static_assert(THREADS >= 32 * kBulkIssuers, "a warp per bulk-store issuer");
@@ -128,11 +135,17 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
     __shared__ float s_win_hi[W], s_win_lo[W];
     const P pipe{smem};
     const int tid = threadIdx.x;
-    uint64_t *status = reinterpret_cast<uint64_t *>(ws + kStatusOff);
+    uint64_t *status = reinterpret_cast<uint64_t *>(ws + kStatusOff) + plan.region;
 
     if (tid == 0) pipe.init();
     __syncthreads();
     if (tid == 0) pipe.prime(op.srcs, TE, n, num_tiles);
+    if (plan.clear_words != 0u) {
+        // The next pass's words, which no tile of this pass reads or writes.
+        uint64_t *next = reinterpret_cast<uint64_t *>(ws + kStatusOff) + plan.clear_region;
+        for (uint32_t j = blockIdx.x * THREADS + tid; j < plan.clear_words; j += gridDim.x * THREADS)
+            next[j] = 0ull;
+    }
 
     uint32_t run_u = 0u;     // inclusive prefix of the tile before the previous one
     float run_h = 0.0f, run_l = 0.0f;  // the same for float32, as a float pair

@@ -313,18 +313,23 @@ cudaError_t run_partition_pipe(const uint32_t *kin, const uint32_t *vin, uint32_
     if (vec) {
         gcd::PartitionOp<PT, PR, Pred, true, VALS> op{};
         fill(op);
-        return gcd::launch_pipeline<PT, PS>(op, n, ws, s, o.timeout_ns);
+        return gcd::launch_pipeline<PT, PS>(op, n, ws, s, o);
     }
     gcd::PartitionOp<PT, PR, Pred, false, VALS> op{};
     fill(op);
-    return gcd::launch_pipeline<PT, PS>(op, n, ws, s, o.timeout_ns);
+    return gcd::launch_pipeline<PT, PS>(op, n, ws, s, o);
 }
 
+// *piped (optional) says whether the persistent kernel ran; the fallback
+// kernels clear their own status words (region 0) with a memset and ignore
+// o's status plan.
 template <class Pred, bool VALS>
 cudaError_t run_partition_pass(const uint32_t *kin, const uint32_t *vin, uint32_t *kout,
                                uint32_t *vout, uint32_t n, const uint32_t *true_total, Pred pred,
-                               uint8_t *ws, cudaStream_t s, const gch::LaunchOpts &o, bool split)
+                               uint8_t *ws, cudaStream_t s, const gch::LaunchOpts &o, bool split,
+                               bool *piped = nullptr)
 {
+    if (piped != nullptr) *piped = false;
     if (gch::aligned16(kin) && (!VALS || gch::aligned16(vin)) && !o.skip_first_tile) {
         cudaError_t e;
         if (split)
@@ -333,7 +338,10 @@ cudaError_t run_partition_pass(const uint32_t *kin, const uint32_t *vin, uint32_
         else
             e = run_partition_pipe<gch::kPartPipeThreads, gch::kPartPipeRows, gch::kPartPipeStages,
                                    Pred, VALS>(kin, vin, kout, vout, n, true_total, pred, ws, s, o);
-        if (e == cudaSuccess) return e;
+        if (e == cudaSuccess) {
+            if (piped != nullptr) *piped = true;
+            return e;
+        }
         (void)cudaGetLastError();  // cooperative grid refused: one tile per CTA instead
     }
     constexpr int PT = gch::kPartThreads, PR = gch::kPartRows;
@@ -468,23 +476,41 @@ cudaError_t launch_split_radix(const uint32_t *keys_in, const uint32_t *vals_in,
         src_k = tmp_k;
         src_v = vals ? tmp_v : nullptr;
     }
+    // The passes share one memset of their status words: pass p publishes in
+    // region p % 2 of the status area (2 T words, which the workspace holds)
+    // and clears the other region for pass p + 1.  A pass that falls back to
+    // the one-tile-per-CTA kernels leaves region 0 to a fresh memset.
+    const uint32_t split_tiles = uint32_t(ceil_div(n, split_tile_elems()));
+    const bool regions = 2ull * split_tiles <= max_tiles(n);
+    if (regions && (e = reset_tiles(ws, 2u * split_tiles, s, false)) != cudaSuccess) return e;
     for (int p = 0; p < passes; ++p) {
+        LaunchOpts po = o;
+        if (regions) {
+            po.reset_status = false;
+            po.status_region = uint32_t(p % 2) * split_tiles;
+            po.clear_region = uint32_t((p + 1) % 2) * split_tiles;
+            po.clear_words = (p + 1 < passes) ? split_tiles : 0u;
+        }
+        bool piped = true;
         // The last pass writes the output; earlier ones alternate so that it does.
         const bool to_out = ((passes - 1 - p) % 2) == 0;
         uint32_t *dst_k = to_out ? keys_out : tmp_k;
         uint32_t *dst_v = vals ? (to_out ? vals_out : tmp_v) : nullptr;
         const int bit = begin_bit + p;
-        const uint32_t *T = reinterpret_cast<const uint32_t *>(ws + kHdrBitZeros + 4 * bit);
+        const uint32_t *zeros = reinterpret_cast<const uint32_t *>(ws + kHdrBitZeros + 4 * bit);
         if (keyed) {
             const gcd::PredKeyBitClear pred{uint32_t(bit), key_neg, (key_flip >> bit) & 1u};
-            e = vals ? run_partition_pass<gcd::PredKeyBitClear, true>(src_k, src_v, dst_k, dst_v, n, T, pred, ws, s, o, true)
-                     : run_partition_pass<gcd::PredKeyBitClear, false>(src_k, nullptr, dst_k, nullptr, n, T, pred, ws, s, o, true);
+            e = vals ? run_partition_pass<gcd::PredKeyBitClear, true>(src_k, src_v, dst_k, dst_v, n, zeros, pred, ws, s, po, true, &piped)
+                     : run_partition_pass<gcd::PredKeyBitClear, false>(src_k, nullptr, dst_k, nullptr, n, zeros, pred, ws, s, po, true, &piped);
         } else {
             const gcd::PredBitClear pred{uint32_t(bit)};
-            e = vals ? run_partition_pass<gcd::PredBitClear, true>(src_k, src_v, dst_k, dst_v, n, T, pred, ws, s, o, true)
-                     : run_partition_pass<gcd::PredBitClear, false>(src_k, nullptr, dst_k, nullptr, n, T, pred, ws, s, o, true);
+            e = vals ? run_partition_pass<gcd::PredBitClear, true>(src_k, src_v, dst_k, dst_v, n, zeros, pred, ws, s, po, true, &piped)
+                     : run_partition_pass<gcd::PredBitClear, false>(src_k, nullptr, dst_k, nullptr, n, zeros, pred, ws, s, po, true, &piped);
         }
         if (e != cudaSuccess) return e;
+        if (regions && !piped && p + 1 < passes &&
+            (e = reset_tiles(ws, 2u * split_tiles, s, false)) != cudaSuccess)
+            return e;
         src_k = dst_k;
         src_v = dst_v;
     }

@@ -157,7 +157,7 @@ cudaError_t launch_scan_pipe(const uint32_t *in, uint32_t *out, uint32_t *total,
 {
     using Op = gcd::ScanOp<kScanPipeThreads, kScanPipeRows, F32, OUT_VEC, INCL>;
     Op op{{in}, out, total};
-    return gcd::launch_pipeline<kScanPipeThreads, kScanPipeStages>(op, n, ws, s, o.timeout_ns);
+    return gcd::launch_pipeline<kScanPipeThreads, kScanPipeStages>(op, n, ws, s, o);
 }
 
 template <bool INCL>

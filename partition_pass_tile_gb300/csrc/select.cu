@@ -140,10 +140,10 @@ cudaError_t dispatch_select(const uint32_t *in, uint32_t *out, uint32_t *count, 
         cudaError_t e;
         if (gch::aligned16(out)) {
             gcd::SelectOp<PT, PR, Pred, true> op{{in}, out, count, pred};
-            e = gcd::launch_pipeline<PT, PS>(op, n, ws, s, o.timeout_ns);
+            e = gcd::launch_pipeline<PT, PS>(op, n, ws, s, o);
         } else {
             gcd::SelectOp<PT, PR, Pred, false> op{{in}, out, count, pred};
-            e = gcd::launch_pipeline<PT, PS>(op, n, ws, s, o.timeout_ns);
+            e = gcd::launch_pipeline<PT, PS>(op, n, ws, s, o);
         }
         if (e == cudaSuccess) return e;
         (void)cudaGetLastError();  // cooperative grid refused: one tile per CTA instead
