@@ -29,6 +29,24 @@ gc_status gc_testing_select_if_skip_tile0(const void *d_in, void *d_out, uint32_
                                           size_t ws_bytes, uint64_t timeout_ns,
                                           cudaStream_t stream);
 
+/*
+ * gc_exclusive_scan with a stalled start barrier.  A persistent kernel clears
+ * its own status words and then waits at a start barrier in the workspace
+ * header until every CTA has arrived; this hook first marks the barrier's
+ * arrival counter the way a barrier wait that ran out leaves it, so no CTA
+ * of this call ever sees the barrier complete.  Each CTA's wait gives up
+ * after timeout_ns nanoseconds of device time, records GC_ERR_TIMEOUT and
+ * carries on.  Requires a 16-byte-aligned d_in (the persistent kernel's
+ * path) and n >= 1; otherwise GC_ERR_INVALID_VALUE, and argument errors as
+ * gc_exclusive_scan.  The output is undefined; gc_query_device_status then
+ * returns GC_ERR_TIMEOUT and clears the barrier's words, after which the
+ * workspace is fit for the next call.
+ */
+gc_status gc_testing_exclusive_scan_stalled_barrier(const void *d_in, void *d_out, void *d_total,
+                                                    size_t n, gc_dtype dtype, void *d_ws,
+                                                    size_t ws_bytes, uint64_t timeout_ns,
+                                                    cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

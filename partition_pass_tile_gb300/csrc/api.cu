@@ -3,6 +3,7 @@
 // GPU before every argument has been checked, so argument errors are
 // reported without any CUDA call.
 #include <cstring>
+#include <mutex>
 
 #include "../../include/gc.h"
 #include "../../include/gc_testing.h"
@@ -21,8 +22,10 @@ cudaError_t reset_tiles(uint8_t *ws, size_t tiles, cudaStream_t s, bool skip_fir
 
 cudaError_t clear_accumulators(uint8_t *ws, cudaStream_t s)
 {
-    // [0, 8) is the error word and its tile; the rest of the header is scratch.
-    return cudaMemsetAsync(ws + 8, 0, kHeaderBytes - 8, s);
+    // [0, 8) is the error word and its tile, [kHdrBarArrive, kHeaderBytes)
+    // the start barrier's counter and the tile counter; the rest of the
+    // header is scratch (the barrier's epoch among it: any value will do).
+    return cudaMemsetAsync(ws + 8, 0, kHdrBarArrive - 8, s);
 }
 
 int sm_count()
@@ -42,14 +45,41 @@ int sm_count()
 
 int persistent_grid(const void *kernel, int threads, size_t smem, uint32_t tiles)
 {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-        cudaSuccess)
-        return -1;
+    // A kernel's shared-memory attribute and occupancy do not change while the
+    // process runs: set and query them once per (kernel, device, shape).
+    struct Entry {
+        const void *kernel;
+        int dev, threads;
+        size_t smem;
+        int per_sm;
+    };
+    static std::mutex mu;
+    static Entry cache[128];
+    static int used = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) !=
-            cudaSuccess ||
-        per_sm <= 0)
-        return -1;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < used; ++i) {
+            const Entry &c = cache[i];
+            if (c.kernel == kernel && c.dev == dev && c.threads == threads && c.smem == smem) {
+                per_sm = c.per_sm;
+                break;
+            }
+        }
+    }
+    if (per_sm == 0) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+            cudaSuccess)
+            return -1;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) !=
+                cudaSuccess ||
+            per_sm <= 0)
+            return -1;
+        std::lock_guard<std::mutex> lock(mu);
+        if (used < 128) cache[used++] = Entry{kernel, dev, threads, smem, per_sm};
+    }
     const long long grid = (long long)per_sm * sm_count();
     return int(grid < (long long)tiles ? grid : (long long)tiles);
 }
@@ -211,7 +241,7 @@ gc_status gc_workspace_init(void *d_ws, size_t ws_bytes, cudaStream_t stream)
 
 static gc_status scan_entry(const void *d_in, void *d_out, void *d_total, size_t n,
                             gc_dtype dtype, void *d_ws, size_t ws_bytes, cudaStream_t stream,
-                            bool inclusive)
+                            bool inclusive, const LaunchOpts &o = LaunchOpts{})
 {
     gc_status st = check_common(d_in, d_out, n, d_ws, ws_bytes, GC_OP_EXCLUSIVE_SCAN, dtype);
     if (st != GC_OK) return st;
@@ -225,7 +255,7 @@ static gc_status scan_entry(const void *d_in, void *d_out, void *d_total, size_t
     if (n == 0)
         return d_total ? from_cuda(cudaMemsetAsync(d_total, 0, 4, stream)) : GC_OK;
     return from_cuda(launch_scan(d_in, d_out, d_total, uint32_t(n), dtype,
-                                 static_cast<uint8_t *>(d_ws), stream, LaunchOpts{}, inclusive));
+                                 static_cast<uint8_t *>(d_ws), stream, o, inclusive));
 }
 
 gc_status gc_exclusive_scan(const void *d_in, void *d_out, void *d_total, size_t n,
@@ -403,8 +433,13 @@ gc_status gc_query_device_status(void *d_ws, cudaStream_t stream)
     if (cudaMemcpy(&err, d_ws, sizeof err, cudaMemcpyDeviceToHost) != cudaSuccess)
         return GC_ERR_CUDA;
     if (err != 0) {
+        // The error word and its tile, and the start barrier's counter (a
+        // wait that ran out leaves it marked so that no later barrier can
+        // complete early).
         const uint32_t zero[2] = {0, 0};
-        if (cudaMemcpy(d_ws, zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+        uint8_t *ws = static_cast<uint8_t *>(d_ws);
+        if (cudaMemcpy(ws, zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess ||
+            cudaMemcpy(ws + kHdrBarArrive, zero, sizeof(uint32_t), cudaMemcpyHostToDevice) != cudaSuccess)
             return GC_ERR_CUDA;
         return (err == GC_ERR_TIMEOUT || err == GC_ERR_DEVICE_CHECK) ? gc_status(err) : GC_ERR_CUDA;
     }
@@ -421,6 +456,23 @@ gc_status gc_testing_select_if_skip_tile0(const void *d_in, void *d_out, uint32_
     o.timeout_ns = timeout_ns;
     o.skip_first_tile = true;
     return select_like(false, d_in, d_out, d_count, n, dtype, pred, d_ws, ws_bytes, stream, o);
+}
+
+gc_status gc_testing_exclusive_scan_stalled_barrier(const void *d_in, void *d_out, void *d_total,
+                                                    size_t n, gc_dtype dtype, void *d_ws,
+                                                    size_t ws_bytes, uint64_t timeout_ns,
+                                                    cudaStream_t stream)
+{
+    gc_status st = check_common(d_in, d_out, n, d_ws, ws_bytes, GC_OP_EXCLUSIVE_SCAN, dtype);
+    if (st != GC_OK) return st;
+    if (n == 0 || !aligned16(d_in)) return GC_ERR_INVALID_VALUE;
+    // The top byte of the little-endian arrival counter: the mark a barrier
+    // wait that ran out leaves.
+    uint8_t *ws = static_cast<uint8_t *>(d_ws);
+    if (cudaMemsetAsync(ws + kHdrBarArrive + 3, 0x80, 1, stream) != cudaSuccess) return GC_ERR_CUDA;
+    LaunchOpts o;
+    o.timeout_ns = timeout_ns;
+    return scan_entry(d_in, d_out, d_total, n, dtype, d_ws, ws_bytes, stream, false, o);
 }
 
 }  // extern "C"

@@ -25,16 +25,21 @@ namespace gcd {
 // then, float32 scan:  one double inclusive prefix per tile
 // radix:               the key and payload ping-pong buffers (see radix.cu)
 //
-// Each call clears the tile counter and its T status words with one
-// cudaMemsetAsync of [kTileCtrOff, 512 + 8 T) before its kernel, so a status
-// word is never read with contents from an earlier call.
+// A persistent call clears its T status words inside its kernel, before a
+// start barrier that every CTA passes before it publishes or reads one
+// (bar_arrive / bar_wait below); the one-tile-per-CTA kernels have the tile
+// counter and their status words cleared by one cudaMemsetAsync of
+// [kTileCtrOff, 512 + 8 T) first.  Either way a status word is never read
+// with contents from an earlier call.
 constexpr uint32_t kHdrError = 0;        // u32: first device failure (gc_status), 0 = none
 constexpr uint32_t kHdrErrorTile = 4;    // u32: tile whose wait gave up
 constexpr uint32_t kHdrReduceCtr = 8;    // u32: CTAs finished in a count pre-pass (self-resetting)
 constexpr uint32_t kHdrCountTrue = 12;   // u32: partition: elements the predicate keeps
 constexpr uint32_t kHdrCountAcc = 16;    // u32: count pre-pass accumulator (reset by the last CTA)
+constexpr uint32_t kHdrBarEpoch = 32;    // u32: start barriers completed (any value will do)
 constexpr uint32_t kHdrBitAcc = 64;      // u32[32]: radix: keys with bit b set, accumulating
 constexpr uint32_t kHdrBitZeros = 192;   // u32[32]: radix: keys with bit b clear
+constexpr uint32_t kHdrBarArrive = 496;  // u32: CTAs arrived at a start barrier (self-resetting)
 constexpr uint32_t kTileCtrOff = 504;    // u32: next tile id (cleared with the status words)
 constexpr uint32_t kStatusOff = 512;
 constexpr uint32_t kHeaderBytes = 512;
@@ -96,6 +101,18 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
+__device__ __forceinline__ uint32_t ld_relaxed_gpu_u32(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_u32(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Records the first device-side failure in the workspace header.
 __device__ __forceinline__ void record_error(uint8_t *ws, uint32_t code, uint32_t tile)
 {
@@ -107,6 +124,69 @@ __device__ __forceinline__ void record_error(uint8_t *ws, uint32_t code, uint32_
 constexpr uint32_t kFullMask = 0xffffffffu;
 constexpr uint32_t kTimeoutCode = 6;      // GC_ERR_TIMEOUT
 constexpr uint32_t kDeviceCheckCode = 7;  // GC_ERR_DEVICE_CHECK
+
+// ---------------------------------------------------------------- start barrier
+//
+// A persistent call clears its own status words; this barrier keeps every
+// publish and every read of a status word behind every CTA's share of the
+// clear.  Thread 0 of each CTA reads the epoch word (bar_epoch) before its
+// CTA arrives, and arrives (bar_arrive) once the whole CTA has cleared: one
+// release add on the arrival counter.  The CTA whose add completes the count
+// sets the counter back to 0 (so the zero-filled workspace and every
+// completed barrier leave it at 0) and releases the epoch's next value; the
+// others wait to acquire a changed epoch (bar_wait), the caller first waiting
+// for its first tile's load so that the two latencies overlap.  A CTA
+// barrier after that wait orders every thread's later accesses.  Every CTA
+// reads the epoch before it arrives and the epoch changes only after the
+// last arrival, so all of them read the same value.  The counter and the
+// epoch sit in different 128-byte lines, so the waiting CTAs' polls of the
+// one do not queue behind the adds on the other.
+//
+// The wait is bounded: past timeout_ns a CTA records GC_ERR_TIMEOUT (error
+// tile kBarrierErrorTile), sets the counter's top bit so that no later call's
+// barrier can complete on a count left over from this one (each times out
+// and reports instead, until gc_query_device_status clears the counter), and
+// carries on.
+constexpr uint32_t kBarPoison = 0x80000000u;
+constexpr uint32_t kBarrierErrorTile = 0xfffffffeu;
+
+__device__ __forceinline__ uint32_t bar_epoch(uint8_t *ws)
+{
+    return ld_relaxed_gpu_u32(hdr_u32(ws, kHdrBarEpoch));
+}
+
+// Returns true if this CTA completed the barrier (nothing to wait for).
+__device__ __forceinline__ bool bar_arrive(uint8_t *ws, uint32_t epoch)
+{
+    uint32_t *arrive = hdr_u32(ws, kHdrBarArrive);
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(arrive) : "memory");
+    if (old != gridDim.x - 1u) return false;
+    st_relaxed_gpu_u32(arrive, 0u);
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(hdr_u32(ws, kHdrBarEpoch)), "r"(epoch + 1u)
+                 : "memory");
+    return true;
+}
+
+__device__ __forceinline__ void bar_wait(uint8_t *ws, uint32_t epoch, uint64_t timeout_ns)
+{
+    const uint32_t *ep = hdr_u32(ws, kHdrBarEpoch);
+    auto changed = [&]() {
+        uint32_t v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ep) : "memory");
+        return v != epoch;
+    };
+    if (changed()) return;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t spins = 0; !changed(); ++spins) {
+        if (spins >= 8) __nanosleep(64);
+        if (global_timer_ns() - t0 > timeout_ns) {
+            record_error(ws, kTimeoutCode, kBarrierErrorTile);
+            atomicOr(hdr_u32(ws, kHdrBarArrive), kBarPoison);
+            return;
+        }
+    }
+}
 
 template <class V>
 __device__ __forceinline__ V warp_sum(V v)

@@ -113,6 +113,7 @@ constexpr uint32_t tile_elems(int threads, int rows) { return uint32_t(threads) 
 // workspace stays valid whatever tile shape a build picks.
 constexpr uint32_t kMinTileElems = 2048;
 constexpr size_t kHeaderBytes = 512;
+constexpr size_t kHdrBarArrive = 496;  // u32: the persistent kernels' start-barrier counter
 constexpr size_t kTileCtrOff = 504;
 
 inline size_t ceil_div(size_t a, size_t b) { return (a + b - 1) / b; }
@@ -136,11 +137,12 @@ inline size_t digit_table_bytes(size_t n) { return align_up(4 * 256 * ceil_div(n
 struct LaunchOpts {
     uint64_t timeout_ns = 1000000000ull;  // a look-back wait gives up after this long
     bool skip_first_tile = false;        // test hook: no CTA ever takes tile 0
-    // Status words of a persistent kernel.  By default a call clears its own
-    // (region 0) with a memset first.  A caller that runs many passes in a
-    // row (the radix split) may instead give each pass the region starting at
-    // word status_region, already clear, and have it clear clear_words words
-    // from clear_region on for the next pass: then no memset runs.
+    // Status words of a persistent kernel, starting at word status_region of
+    // the status area.  By default the kernel clears them itself behind its
+    // start barrier; reset_status = false says they are clear already.  A
+    // caller that runs many passes in a row (the radix split) has each pass
+    // clear clear_words words from clear_region on for the next one, which
+    // then needs neither a clear nor a barrier.
     bool reset_status = true;
     uint32_t status_region = 0, clear_region = 0, clear_words = 0;
 };
@@ -150,7 +152,8 @@ struct LaunchOpts {
 cudaError_t reset_tiles(uint8_t *ws, size_t tiles, cudaStream_t s, bool skip_first_tile);
 
 // Clears the header words of the count pre-pass and the radix histogram
-// (everything in the header except the error word) before those kernels.
+// (the header but its error word, start-barrier words and tile counter)
+// before those kernels.
 cudaError_t clear_accumulators(uint8_t *ws, cudaStream_t s);
 
 // Launchers.  All arguments were validated by api.cu; n >= 1.

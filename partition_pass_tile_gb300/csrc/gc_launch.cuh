@@ -24,21 +24,17 @@ pipeline_kernel(Op op, uint32_t n, uint32_t num_tiles, uint8_t *ws, uint64_t tim
     pipeline_run<THREADS, STAGES>(op, smem, n, num_tiles, ws, timeout_ns, plan);
 }
 
-// Clears this call's tile status words and launches the cooperative
-// persistent grid (as many CTAs as fit, at most one per tile).  Returns the
-// launch error; a refused cooperative launch (the device cannot hold the
-// grid right now) lets the caller fall back to a one-tile-per-CTA kernel.
+// Launches the cooperative persistent grid (as many CTAs as fit, at most one
+// per tile), which clears its own tile status words unless o says they are
+// clear already.  Returns the launch error; a refused cooperative launch (the
+// device cannot hold the grid right now) lets the caller fall back to a
+// one-tile-per-CTA kernel.
 template <int THREADS, int STAGES, class Op>
 cudaError_t launch_pipeline(const Op &op, uint32_t n, uint8_t *ws, cudaStream_t s,
                             const gch::LaunchOpts &o)
 {
     uint32_t tiles = uint32_t(gch::ceil_div(n, Op::kTileElems));
-    if (o.reset_status) {
-        const cudaError_t e = gch::reset_tiles(ws, tiles, s, false);
-        if (e != cudaSuccess) return e;
-    }
-    StatusPlan plan{o.reset_status ? 0u : o.status_region, o.clear_region,
-                    o.reset_status ? 0u : o.clear_words};
+    StatusPlan plan{o.status_region, o.reset_status ? 1u : 0u, o.clear_region, o.clear_words};
     uint64_t timeout_ns = o.timeout_ns;
     auto kernel = pipeline_kernel<THREADS, STAGES, Op>;
     constexpr uint32_t smem = Op::template PipeT<STAGES>::kBytes;

@@ -116,9 +116,11 @@ __device__ __forceinline__ void window_finish_ff(const uint64_t *status, uint32_
 //   op.finish(p): outputs from the carried offsets;
 //   a barrier, then p's stage is re-armed.
 // Where a persistent call's status words are (word offset from the status
-// area) and which words, already unused, it clears for the call after it.
+// area), whether the kernel clears them itself first (behind the start
+// barrier; otherwise they are clear already), and which words, unused by
+// this call, it clears for the call after it.
 struct StatusPlan {
-    uint32_t region, clear_region, clear_words;
+    uint32_t region, self_clear, clear_region, clear_words;
 };
 
 template <int THREADS, int STAGES, class Op>
@@ -137,6 +139,9 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
     const int tid = threadIdx.x;
     uint64_t *status = reinterpret_cast<uint64_t *>(ws + kStatusOff) + plan.region;
 
+    const bool self_clear = plan.self_clear != 0u;
+    uint32_t epoch = 0u;  // thread 0: the start barrier's epoch, read before arriving
+    if (tid == 0 && self_clear) epoch = bar_epoch(ws);
     if (tid == 0) pipe.init();
     __syncthreads();
     if (tid == 0) pipe.prime(op.srcs, TE, n, num_tiles);
@@ -146,15 +151,56 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
         for (uint32_t j = blockIdx.x * THREADS + tid; j < plan.clear_words; j += gridDim.x * THREADS)
             next[j] = 0ull;
     }
+    bool bar_pending = false;  // thread 0: arrived, the barrier not yet seen complete
+    if (self_clear) {
+        // This call's own words, while the primed loads are in flight.
+        for (uint32_t j = blockIdx.x * THREADS + tid; j < num_tiles; j += gridDim.x * THREADS)
+            status[j] = 0ull;
+        __syncthreads();
+        if (tid == 0) bar_pending = !bar_arrive(ws, epoch);
+    }
 
     uint32_t run_u = 0u;     // inclusive prefix of the tile before the previous one
     float run_h = 0.0f, run_l = 0.0f;  // the same for float32, as a float pair
     uint32_t prev_agg = 0u;  // aggregate bits of the previous tile
     typename Op::Carry cur{}, prv{};  // per-thread results of a reduction kept for its finish
-    for (uint32_t k = 0;; ++k) {
+
+    // Iteration 0, peeled: the CTA's first tile is reduced while the start
+    // barrier completes, and its aggregate is published once it has.
+    if (blockIdx.x >= num_tiles) {
+        if (tid == 0 && bar_pending) bar_wait(ws, epoch, timeout_ns);
+        return;
+    }
+    {
+        const uint32_t tile = blockIdx.x;
+        mbar_wait(pipe.bar(0), 0u, ws, timeout_ns);
+        const uint32_t staged = staged_elems(tile, TE, n);
+        uint32_t first_bits = 0u;
+        auto publish = [&](uint32_t bits) {
+            if (tid == 0) {
+                if (self_clear)
+                    first_bits = bits;
+                else
+                    publish_aggregate(status, tile, bits);
+            }
+        };
+        if (staged == TE)
+            prev_agg = op.template reduce<true>(pipe, 0, tile * TE, staged, n, cur, publish);
+        else
+            prev_agg = op.template reduce<false>(pipe, 0, tile * TE, staged, n, cur, publish);
+        if (self_clear) {
+            if (tid == 0) {
+                if (bar_pending) bar_wait(ws, epoch, timeout_ns);
+                publish_aggregate(status, tile, first_bits);
+            }
+            __syncthreads();  // every thread's first status read comes after the barrier
+        }
+        prv = cur;
+    }
+    for (uint32_t k = 1;; ++k) {
         const uint32_t tile = blockIdx.x + k * gridDim.x;
         const bool have = tile < num_tiles;
-        const bool have_prev = k > 0;
+        const bool have_prev = true;
         const uint32_t prev = tile - gridDim.x;
 
         WindowLoads wl;

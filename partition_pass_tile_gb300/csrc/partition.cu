@@ -476,17 +476,18 @@ cudaError_t launch_split_radix(const uint32_t *keys_in, const uint32_t *vals_in,
         src_k = tmp_k;
         src_v = vals ? tmp_v : nullptr;
     }
-    // The passes share one memset of their status words: pass p publishes in
-    // region p % 2 of the status area (2 T words, which the workspace holds)
-    // and clears the other region for pass p + 1.  A pass that falls back to
-    // the one-tile-per-CTA kernels leaves region 0 to a fresh memset.
+    // Pass p publishes in region p % 2 of the status area (2 T words, which
+    // the workspace holds) and clears the other region for pass p + 1, so
+    // only the first pass clears its own words (behind its start barrier).
+    // A pass that falls back to the one-tile-per-CTA kernels leaves both
+    // regions to a memset.
     const uint32_t split_tiles = uint32_t(ceil_div(n, split_tile_elems()));
     const bool regions = 2ull * split_tiles <= max_tiles(n);
-    if (regions && (e = reset_tiles(ws, 2u * split_tiles, s, false)) != cudaSuccess) return e;
+    bool fresh = true;  // the next pass's region still needs its own clear
     for (int p = 0; p < passes; ++p) {
         LaunchOpts po = o;
         if (regions) {
-            po.reset_status = false;
+            po.reset_status = fresh;
             po.status_region = uint32_t(p % 2) * split_tiles;
             po.clear_region = uint32_t((p + 1) % 2) * split_tiles;
             po.clear_words = (p + 1 < passes) ? split_tiles : 0u;
@@ -508,6 +509,7 @@ cudaError_t launch_split_radix(const uint32_t *keys_in, const uint32_t *vals_in,
                      : run_partition_pass<gcd::PredBitClear, false>(src_k, nullptr, dst_k, nullptr, n, zeros, pred, ws, s, po, true, &piped);
         }
         if (e != cudaSuccess) return e;
+        fresh = false;
         if (regions && !piped && p + 1 < passes &&
             (e = reset_tiles(ws, 2u * split_tiles, s, false)) != cudaSuccess)
             return e;

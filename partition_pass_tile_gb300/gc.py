@@ -73,6 +73,7 @@ def load(path: str | Path | None = None) -> ctypes.CDLL:
         "gc_select_if_atomic": ([V, V, V, Z, I, I, V, Z, V], S),
         "gc_query_device_status": ([V, V], S),
         "gc_testing_select_if_skip_tile0": ([V, V, V, Z, I, I, V, Z, U64, V], S),
+        "gc_testing_exclusive_scan_stalled_barrier": ([V, V, V, Z, I, V, Z, U64, V], S),
         "gc_inclusive_scan": ([V, V, V, Z, I, V, Z, V], S),
         "gc_select_if_pred": ([V, V, V, Z, I, ctypes.POINTER(Predicate), V, Z, V], S),
         "gc_partition_pred": ([V, V, V, Z, I, ctypes.POINTER(Predicate), V, Z, V], S),
@@ -314,6 +315,14 @@ def testing_select_if_skip_tile0(x: torch.Tensor, pred, out, count, ws, timeout_
     return int(load().gc_testing_select_if_skip_tile0(
         _ptr(x), _ptr(out), _ptr(count), x.numel(), dtype_code(x), pred_code(pred), _ptr(ws),
         ws.numel(), timeout_ns, _stream(stream)))
+
+
+def testing_exclusive_scan_stalled_barrier(x: torch.Tensor, out, total, ws, timeout_ns: int,
+                                           stream=None) -> int:
+    """Test hook (include/gc_testing.h): returns the launch status."""
+    return int(load().gc_testing_exclusive_scan_stalled_barrier(
+        _ptr(x), _ptr(out), _ptr(total), x.numel(), dtype_code(x), _ptr(ws), ws.numel(),
+        timeout_ns, _stream(stream)))
 
 
 NOALLOC_MAX_ELEMENTS = 1 << 28

@@ -38,7 +38,8 @@ def test_header_declares_the_entry_points():
                  "gc_select_if_atomic", "gc_workspace_bytes", "gc_query_device_status",
                  "gc_status_string", "gc_workspace_init", "gc_tile_elements",
                  "gc_testing_select_if_skip_tile0", "gc_inclusive_scan", "gc_select_if_pred",
-                 "gc_partition_pred", "gc_select_if_noalloc", "gc_radix_sort"]:
+                 "gc_partition_pred", "gc_select_if_noalloc", "gc_radix_sort",
+                 "gc_testing_exclusive_scan_stalled_barrier"]:
         assert want in names
 
 
@@ -119,6 +120,16 @@ def test_scan_validation(lib):
     assert f(IN, OUT, None, 1000, 3, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
     assert f(IN, OUT, None, 1000, gc.F32, WS, 530, None) == E["GC_ERR_WORKSPACE_TOO_SMALL"]
     assert f(None, OUT, None, 1000, gc.I32, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+
+
+def test_stalled_barrier_hook_validation(lib):
+    # Refused before any CUDA call: the hook needs the persistent kernel's
+    # path (a 16-byte-aligned input) and at least one element.
+    E = {v: k for k, v in gc.STATUS.items()}
+    f = lib.gc_testing_exclusive_scan_stalled_barrier
+    assert f(IN, OUT, None, 0, gc.I32, WS, BIG, 1000, None) == E["GC_ERR_INVALID_VALUE"]
+    assert f(IN + 4, OUT, None, 1000, gc.I32, WS, BIG, 1000, None) == E["GC_ERR_INVALID_VALUE"]
+    assert f(IN, OUT, None, 1000, gc.I32, WS + 8, BIG, 1000, None) == E["GC_ERR_MISALIGNED"]
 
 
 def test_pred_validation(lib):

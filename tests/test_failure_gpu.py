@@ -1,7 +1,8 @@
 """Failure detection on the GPU without faulting it.
 
-A look-back wait that can never be satisfied (tile 0 is never taken, planted
-through the gc_testing.h hook) must give up after its time limit, record
+A wait that can never be satisfied, planted through a gc_testing.h hook (a
+look-back on tile 0, which no CTA takes; a start barrier whose counter is
+marked as one that ran out) must give up after its time limit, record
 GC_ERR_TIMEOUT in the workspace and let the kernel finish; the host reads the
 status, and the same workspace and context then work normally.
 """
@@ -46,3 +47,22 @@ def test_testing_hook_rejects_single_tile():
                                          torch.empty(1, dtype=torch.uint32, device="cuda"), ws,
                                          timeout_ns=1_000_000)
     assert st == 1  # GC_ERR_INVALID_VALUE
+
+
+def test_start_barrier_timeout_is_reported_and_recoverable(orc):
+    n = 3_000_017  # several CTAs per SM's worth of tiles: the whole persistent grid
+    x = synth.uniform_i32(n, 22)
+    xd = dev(x)
+    ws = gc.workspace(gc.OP_EXCLUSIVE_SCAN, n)
+    out = torch.empty_like(xd)
+    tot = torch.empty(1, dtype=torch.int32, device="cuda")
+    st = gc.testing_exclusive_scan_stalled_barrier(xd, out, tot, ws, timeout_ns=5_000_000)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert gc.query_device_status(ws) == 6   # GC_ERR_TIMEOUT
+    assert gc.query_device_status(ws) == 0   # read-and-clear, barrier words included
+    want, _ = orc.exclusive_scan(x)
+    for _ in range(2):  # the barrier completes again, call after call
+        out, tot = gc.exclusive_scan(xd, ws=ws)
+        assert np.array_equal(host(out), want)
+        assert gc.query_device_status(ws) == 0

@@ -262,6 +262,31 @@ def test_workspace_reuse_small_sort_then_large_scan(orc):
     assert gc.query_device_status(ws) == 0
 
 
+def test_back_to_back_calls_alternating_inputs(orc):
+    """Persistent calls clear their status words inside the kernel, behind a
+    start barrier.  Back-to-back calls on one workspace with inputs that
+    alternate (so that a status word left by the previous call would give a
+    different prefix), all results kept on the device and checked at the end:
+    a tile that read a word before its clear would show as a wrong prefix."""
+    n = 5_000_011  # more tiles than the persistent grid has CTAs
+    xs = [synth.uniform_i32(n, 31), synth.scan_mod8(n)]
+    ks = [synth.keep_fraction(n, 0.25, 32), synth.keep_fraction(n, 0.75, 33)]
+    xd, kd = [dev(a) for a in xs], [dev(a) for a in ks]
+    ws = gc.workspace(gc.OP_SELECT_IF, n)
+    scans, sels = [], []
+    for i in range(12):
+        scans.append(gc.exclusive_scan(xd[i % 2], ws=ws)[0])
+        sels.append(gc.select_if(kd[i % 2], "nonzero", ws=ws))
+    want_scan = [orc.exclusive_scan(a)[0] for a in xs]
+    want_sel = [orc.select_if(a, O.NONZERO) for a in ks]
+    for i in range(12):
+        assert np.array_equal(host(scans[i]), want_scan[i % 2]), i
+        out, c = sels[i]
+        w = want_sel[i % 2]
+        assert int(host(c)[0]) == w.shape[0] and np.array_equal(host(out)[: w.shape[0]], w), i
+    assert gc.query_device_status(ws) == 0
+
+
 def test_streams_and_empty_inputs():
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
