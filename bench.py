@@ -590,7 +590,7 @@ def run_gc(args):
                      "peak_nominal": NOMINAL_HBM_GBS,
                      "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                      "duration_note": "radix32 call time / 32: includes the histogram pass "
-                                      "and the one status-word clear of all 32 splits"},
+                                      "(the splits clear their own status words)"},
         "clocks": clocks.summary(),
         "e2e": {"value": round(sum_over_ranks(elems_step, world, dev) / (e2e_ms / 1e3) / 1e9, 3),
                 "unit": "Gelem/s", "ms_per_step": round(e2e_ms, 3),
