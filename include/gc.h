@@ -293,7 +293,10 @@ gc_status gc_select_if_atomic(const void *d_in, void *d_out, uint32_t *d_count,
  * the array: each clears what must start at zero on its own stream, and
  * calls that can overlap on the GPU (different streams with no ordering
  * between them) race on it.  Device-side timeouts of this entry point are
- * recorded in that array, which no query reads.  No allocation of any kind.
+ * recorded in that array, which no query reads; a start-barrier timeout
+ * (only possible if the cooperative grid were not all resident) would leave
+ * the array's barrier marked, and every later call in the process would then
+ * wait out its time limit (1 s) before finishing.  No allocation of any kind.
  */
 #define GC_NOALLOC_MAX_ELEMENTS 268435456u
 gc_status gc_select_if_noalloc(const void *d_in, void *d_out, uint32_t *d_count,
@@ -303,10 +306,14 @@ gc_status gc_select_if_noalloc(const void *d_in, void *d_out, uint32_t *d_count,
 /*
  * SYNCHRONOUS.  Waits for `stream`, then reads and clears the device-side
  * error word of the workspace.  Returns GC_OK, GC_ERR_TIMEOUT if a kernel's
- * look-back wait gave up since the last query, GC_ERR_DEVICE_CHECK if a
- * kernel found an output range outside its buffer (a corrupted workspace) and
- * skipped those stores -- in both cases the outputs of that call are
- * undefined -- or GC_ERR_CUDA if the synchronisation itself failed.
+ * bounded wait (a look-back, a staged load, or the start barrier at which a
+ * persistent kernel's CTAs meet after clearing their status words) gave up
+ * since the last query, GC_ERR_DEVICE_CHECK if a kernel found an output range
+ * outside its buffer (a corrupted workspace) and skipped those stores -- in
+ * both cases the outputs of that call are undefined -- or GC_ERR_CUDA if the
+ * synchronisation itself failed.  After an error it also resets the start
+ * barrier's arrival counter, which a barrier wait that gave up leaves marked
+ * so that later calls time out rather than pass the barrier early.
  */
 gc_status gc_query_device_status(void *d_ws, cudaStream_t stream);
 

@@ -17,10 +17,12 @@
 // Make the first call on a device before any stream capture begins.
 //
 // Every call shares the one array.  Each call clears the parts that must
-// start at zero (the tile counter and its status words) with an async
-// memset on its own stream before its kernel runs; calls whose work can
-// overlap on the GPU (different streams with no ordering between them) race
-// on the array and must not be issued.
+// start at zero on its own stream: the persistent kernel its status words,
+// inside the kernel; the one-tile-per-CTA fallback the tile counter and its
+// status words, with an async memset first.  Calls whose work can overlap on
+// the GPU (different streams with no ordering between them) race on the
+// array and must not be issued.  The array starts zero-filled, as a
+// workspace must.
 #include <cstring>
 #include <mutex>
 
