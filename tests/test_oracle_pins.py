@@ -76,6 +76,24 @@ MUTANTS = [
     ("radix_drops_payload_swap",
      "        t = va; va = vb; vb = t;",
      "        (void)0;"),
+    ("inclusive_scan_u32_stores_before_add",
+     "        running += in[i];\n        out[i] = running;",
+     "        out[i] = running;\n        running += in[i];"),
+    ("inclusive_scan_f32_stores_before_add",
+     "        running += (double)in[i];\n        out[i] = running;",
+     "        out[i] = running;\n        running += (double)in[i];"),
+    ("even_tests_wrong_bit",
+     "    return (bits & 1u) == 0u; /* ORC_EVEN */",
+     "    return (bits & 2u) == 0u; /* ORC_EVEN */"),
+    ("int_nonzero_drops_negatives",
+     "        return bits != 0u;\n    }",
+     "        return (int32_t)bits > 0;\n    }"),
+    ("count_if_skips_last_element",
+     "    for (size_t i = 0; i < n; ++i) c += (size_t)keep(in[i], dtype, pred);",
+     "    for (size_t i = 0; i + 1 < n; ++i) c += (size_t)keep(in[i], dtype, pred);"),
+    ("float_key_negative_mapped_back_wrong",
+     "    if (dtype == ORC_F32) return (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key;",
+     "    if (dtype == ORC_F32) return (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : (key ^ 0x80000000u);"),
 ]
 
 
