@@ -794,43 +794,6 @@ __device__ __forceinline__ uint32_t await_aggregate(const uint64_t *status, uint
     }
 }
 
-// Sum over the aggregates of tiles [lo, hi), read by all THREADS threads and
-// reduced across the CTA (uint32 wrap-around, or float32 aggregates summed in
-// double).  Every thread gets the sum.  s_red: THREADS / 32 slots.
-template <int THREADS>
-__device__ __forceinline__ uint32_t window_sum_u32(const uint64_t *status, uint32_t lo, uint32_t hi,
-                                                   uint8_t *ws, uint32_t tile,
-                                                   uint64_t timeout_ns, uint32_t *s_red)
-{
-    uint32_t sum = 0u;
-    for (uint32_t j = lo + threadIdx.x; j < hi; j += THREADS)
-        sum += await_aggregate(status, j, ws, tile, timeout_ns);
-    sum = warp_sum(sum);
-    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = sum;
-    __syncthreads();
-    uint32_t total = 0u;
-#pragma unroll
-    for (int w = 0; w < THREADS / 32; ++w) total += s_red[w];
-    return total;
-}
-
-template <int THREADS>
-__device__ __forceinline__ double window_sum_f32(const uint64_t *status, uint32_t lo, uint32_t hi,
-                                                 uint8_t *ws, uint32_t tile, uint64_t timeout_ns,
-                                                 double *s_red)
-{
-    double sum = 0.0;
-    for (uint32_t j = lo + threadIdx.x; j < hi; j += THREADS)
-        sum += double(__uint_as_float(await_aggregate(status, j, ws, tile, timeout_ns)));
-    sum = warp_sum(sum);
-    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = sum;
-    __syncthreads();
-    double total = 0.0;
-#pragma unroll
-    for (int w = 0; w < THREADS / 32; ++w) total += s_red[w];
-    return total;
-}
-
 // First tile of the window of tile k (the tiles after this CTA's previous one).
 __device__ __forceinline__ uint32_t window_lo(uint32_t k)
 {
