@@ -578,7 +578,7 @@ def run_gc(args):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "ops": ops_report,
         "next_ops": {k: dict(v, frac_of_peak=round(v["alg_gbs"] / peak, 4)) for k, v in next_ops.items()},
-        "roofline": {"kernel": "partition_kernel<PredBitClear, payload> (one-bit radix split)",
+        "roofline": {"kernel": "pipeline_kernel<256, 3, PartitionOp<256, 4, PredBitClear, VEC, payload>> (one-bit radix split)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs",
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
