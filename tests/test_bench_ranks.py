@@ -64,3 +64,28 @@ def test_two_ranks_over_gloo():
     assert results[0][2] != results[1][2]                  # replicas draw their own batch
     assert '"impl": "reference"' in results[0][3]          # rank 0 prints the reference line
     assert results[1][3] == ""                             # the other rank prints nothing
+
+
+def test_reference_line_fields():
+    """The reference arm's JSON line at one rank: the step's metric and unit,
+    the oracle as its CPU baseline, and an end-to-end figure equal to its
+    value with no host-device copies."""
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.run_reference(bench.parse_args(["--impl", "reference", "--steps", "2", "--warmup", "1",
+                                              "--cpu-sample", "16384", "--n", "8192"]))
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["metric"] == bench.METRIC and line["unit"] == "Gelem/s"
+    assert line["value"] > 0 and line["higher_is_better"] is True
+    assert line["n_gpus"] == 1 and line["steps"] == 2 and line["warmup"] == 1
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == line["value"]
+    assert "4096 elements" in cb["sample"]  # min(cpu_sample / 4, n)
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+    assert line["config"]["sample_n"] == 4096 and line["config"]["n"] == 8192
