@@ -17,6 +17,9 @@ Parity status of each function (what pins it, in ``tests/test_oracle_pins.py``):
   first-difference invariant, brute force.
 * exclusive_scan (float32 -> float64): exact integer prefix of inputs that are
   multiples of 2^-24, closed form for the every-fourth-is-2 input.
+* inclusive_scan (int32/uint32, float32 -> float64): the identity
+  inclusive[i] = exclusive[i] + in[i] against the exclusive forms above, with
+  equal totals; storing an element before adding it fails it.
 * select_if / count_if: printed worked example (CIS 565 compaction log),
   O(n^2) brute-force rank counting, subsequence invariant, all/none kept.
 * partition: brute-force ranks for both halves, permutation + stability
