@@ -445,6 +445,46 @@ def run_gc(args):
         next_ops[name] = {"ms": round(ms, 4), "gelem_s": round(n / ms / 1e6, 2),
                           "alg_gbs": round(nbytes / ms / 1e6, 1)}
 
+    # The comparison the atomic-counter path exists for ("compaction.cu -- Day
+    # 33": its cost should move with the survival rate, the scanned one's
+    # should not): stable select-if against the page's comparator (one atomic
+    # per survivor) and the per-tile variant, at 1 / 50 / 99 % kept, on the
+    # step's arrays.  misplaced = output positions whose element differs from
+    # the stable answer's, reported and never gated (the page's
+    # countOutOfOrder).
+    comparator = {}
+    out_s = torch.empty(n, dtype=torch.int32, device=dev)
+    for key, pname in (("s01", "p01"), ("s50", "p50"), ("s99", "p99")):
+        xs = d[key]
+        m = int(np.count_nonzero(h[key]))
+        variants = {
+            "select_if": lambda: gc.select_if(xs, "nonzero", out=out_s, count=counts[2:3], ws=ws, stream=stream),
+            "atomic_per_survivor": lambda: gc.select_if_atomic(xs, "nonzero", out=out_a, count=counts[3:4], ws=ws, stream=stream),
+            "atomic_per_tile": lambda: gc.select_if_atomic(xs, "nonzero", out=out_b, count=counts[4:5], ws=ws, stream=stream, per_tile=True),
+        }
+        row = {}
+        for vname, fn in variants.items():
+            for _ in range(max(args.warmup, 1)):
+                fn()
+            evn = [(new_ev(), new_ev()) for _ in range(args.steps)]
+            for a_, b_ in evn:
+                a_.record(stream)
+                fn()
+                b_.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = sum(a_.elapsed_time(b_) for a_, b_ in evn) / args.steps
+            nbytes = 4.0 * n + 4.0 * m + 4
+            row[vname] = {"ms": round(ms, 4), "alg_gbs": round(nbytes / ms / 1e6, 1),
+                          "frac_of_peak": round(nbytes / ms / 1e6 / read_peaks()[0], 4)}
+        got_c = counts[2:5].view(torch.int32).cpu().numpy()
+        assert all(int(c) == m for c in got_c), (pname, got_c, m)
+        ref = out_s[:m]
+        row["atomic_per_survivor"]["misplaced"] = int((out_a[:m] != ref).sum().item())
+        row["atomic_per_tile"]["misplaced"] = int((out_b[:m] != ref).sum().item())
+        row["kept"] = m
+        comparator[pname] = row
+    del out_s
+
     # End to end: every step copies its inputs in from pinned host memory and
     # every output (and the counts) back, through the C ABI.  Three streams:
     # host-to-device copies, the kernels, device-to-host copies, ordered by
@@ -578,6 +618,7 @@ def run_gc(args):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "ops": ops_report,
         "next_ops": {k: dict(v, frac_of_peak=round(v["alg_gbs"] / peak, 4)) for k, v in next_ops.items()},
+        "comparator": comparator,
         "roofline": {"kernel": "pipeline_kernel<256, 3, PartitionOp<256, 4, PredBitClear, VEC, payload>> (one-bit radix split)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs",

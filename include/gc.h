@@ -36,8 +36,10 @@
  *                        the standard sign-flip reading of "sort by the
  *                        value" for the other two dtypes.
  *   gc_select_if_atomic  the comparison path: the same survivors and count,
- *                        placed by an atomic counter, in no defined order.
- *                        "compaction.cu -- Day 33" (compactAtomic).
+ *                        placed by an atomic counter (one atomicAdd per
+ *                        survivor), in no defined order.  "compaction.cu --
+ *                        Day 33" (compactAtomic).  gc_select_if_atomic_tile
+ *                        is the same with one atomic per tile.
  *
  * Conventions common to every entry point:
  *
@@ -266,15 +268,34 @@ gc_status gc_radix_sort(const void *d_keys_in, const uint32_t *d_vals_in,
                         cudaStream_t stream);
 
 /*
- * The atomic-counter comparison path: the same survivors and the same
- * *d_count as gc_select_if, in an order the hardware decides (only the
- * multiset of d_out[0, *d_count) is defined).  One atomic per tile of
- * gc_tile_elements(GC_OP_SELECT_IF_ATOMIC) elements on a single counter.
+ * The atomic-counter comparison path of "compaction.cu -- Day 33"
+ * (compactAtomic): every survivor takes its output slot with one atomicAdd
+ * on the single counter *d_count and is written there.  The same survivors
+ * and the same *d_count as gc_select_if, in an order the hardware decides:
+ * only the multiset of d_out[0, *d_count) is defined.  Its cost grows with
+ * the number of survivors, all of which serialise on one address.  The
+ * counter is cleared on the stream before the kernel; the workspace
+ * (gc_workspace_bytes(GC_OP_SELECT_IF_ATOMIC, ...)) is checked but unused.
  */
 gc_status gc_select_if_atomic(const void *d_in, void *d_out, uint32_t *d_count,
                               size_t n, gc_dtype dtype, gc_pred pred,
                               void *d_ws, size_t ws_bytes,
                               cudaStream_t stream);
+
+/*
+ * gc_select_if_atomic with one atomic per tile of
+ * gc_tile_elements(GC_OP_SELECT_IF_ATOMIC) elements instead of one per
+ * survivor: each CTA ranks its tile's survivors, claims a run of that many
+ * slots with one atomicAdd on *d_count and writes the run.  Survivors keep
+ * their input order within a tile; the tiles' runs land in the order their
+ * atomics resolve.  Same arguments, workspace and output contract as
+ * gc_select_if_atomic.  Not on the pages: it shows how much of the
+ * comparator's cost is the one-address serialisation.
+ */
+gc_status gc_select_if_atomic_tile(const void *d_in, void *d_out, uint32_t *d_count,
+                                   size_t n, gc_dtype dtype, gc_pred pred,
+                                   void *d_ws, size_t ws_bytes,
+                                   cudaStream_t stream);
 
 /*
  * gc_select_if without a workspace, for callers that cannot allocate device

@@ -160,16 +160,22 @@ gc_status check_radix_arrays(const void *keys_in, const uint32_t *vals_in, const
     return GC_OK;
 }
 
-gc_status select_like(bool atomic, const void *d_in, void *d_out, uint32_t *d_count, size_t n,
+// Which select-if: the stable one, or the atomic comparison path with one
+// atomic per survivor or per tile.
+enum class SelectKind { Stable, AtomicElem, AtomicTile };
+
+gc_status select_like(SelectKind kind, const void *d_in, void *d_out, uint32_t *d_count, size_t n,
                       gc_dtype dt, gc_pred p, void *d_ws, size_t ws_bytes, cudaStream_t s,
                       const LaunchOpts &o)
 {
+    const bool atomic = kind != SelectKind::Stable;
     const gc_op op = atomic ? GC_OP_SELECT_IF_ATOMIC : GC_OP_SELECT_IF;
     gc_status st = check_select_like(d_in, d_out, d_count, n, dt, p, d_ws, ws_bytes, op);
     if (st != GC_OK) return st;
     if (n == 0) return from_cuda(cudaMemsetAsync(d_count, 0, sizeof(uint32_t), s));
     if (atomic)
-        return from_cuda(launch_select_atomic(d_in, d_out, d_count, uint32_t(n), dt, p, s));
+        return from_cuda(launch_select_atomic(d_in, d_out, d_count, uint32_t(n), dt, p, s,
+                                              kind == SelectKind::AtomicTile));
     return from_cuda(launch_select(d_in, d_out, d_count, uint32_t(n), dt, p,
                                    static_cast<uint8_t *>(d_ws), s, o));
 }
@@ -274,16 +280,24 @@ gc_status gc_select_if(const void *d_in, void *d_out, uint32_t *d_count, size_t 
                        gc_dtype dtype, gc_pred pred, void *d_ws, size_t ws_bytes,
                        cudaStream_t stream)
 {
-    return select_like(false, d_in, d_out, d_count, n, dtype, pred, d_ws, ws_bytes, stream,
-                       LaunchOpts{});
+    return select_like(SelectKind::Stable, d_in, d_out, d_count, n, dtype, pred, d_ws, ws_bytes,
+                       stream, LaunchOpts{});
 }
 
 gc_status gc_select_if_atomic(const void *d_in, void *d_out, uint32_t *d_count, size_t n,
                               gc_dtype dtype, gc_pred pred, void *d_ws, size_t ws_bytes,
                               cudaStream_t stream)
 {
-    return select_like(true, d_in, d_out, d_count, n, dtype, pred, d_ws, ws_bytes, stream,
-                       LaunchOpts{});
+    return select_like(SelectKind::AtomicElem, d_in, d_out, d_count, n, dtype, pred, d_ws,
+                       ws_bytes, stream, LaunchOpts{});
+}
+
+gc_status gc_select_if_atomic_tile(const void *d_in, void *d_out, uint32_t *d_count, size_t n,
+                                   gc_dtype dtype, gc_pred pred, void *d_ws, size_t ws_bytes,
+                                   cudaStream_t stream)
+{
+    return select_like(SelectKind::AtomicTile, d_in, d_out, d_count, n, dtype, pred, d_ws,
+                       ws_bytes, stream, LaunchOpts{});
 }
 
 gc_status gc_partition(const void *d_in, void *d_out, uint32_t *d_count_true, size_t n,
@@ -455,7 +469,8 @@ gc_status gc_testing_select_if_skip_tile0(const void *d_in, void *d_out, uint32_
     LaunchOpts o;
     o.timeout_ns = timeout_ns;
     o.skip_first_tile = true;
-    return select_like(false, d_in, d_out, d_count, n, dtype, pred, d_ws, ws_bytes, stream, o);
+    return select_like(SelectKind::Stable, d_in, d_out, d_count, n, dtype, pred, d_ws, ws_bytes,
+                       stream, o);
 }
 
 gc_status gc_testing_exclusive_scan_stalled_barrier(const void *d_in, void *d_out, void *d_total,

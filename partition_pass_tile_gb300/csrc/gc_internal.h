@@ -172,8 +172,10 @@ cudaError_t launch_partition_cmp(const void *in, void *out, uint32_t *count_true
                                  const LaunchOpts &o);
 cudaError_t launch_select(const void *in, void *out, uint32_t *count, uint32_t n, gc_dtype dt,
                           gc_pred p, uint8_t *ws, cudaStream_t s, const LaunchOpts &o);
+// per_tile: one atomic per tile (gc_select_if_atomic_tile); otherwise one
+// per survivor (gc_select_if_atomic).
 cudaError_t launch_select_atomic(const void *in, void *out, uint32_t *count, uint32_t n,
-                                 gc_dtype dt, gc_pred p, cudaStream_t s);
+                                 gc_dtype dt, gc_pred p, cudaStream_t s, bool per_tile);
 cudaError_t launch_partition(const void *in, void *out, uint32_t *count_true, uint32_t n,
                              gc_dtype dt, gc_pred p, uint8_t *ws, cudaStream_t s,
                              const LaunchOpts &o);

@@ -20,6 +20,8 @@
 //      and the CTA writes its survivors as one contiguous run with 128-bit
 //      stores (scalar stores only for the partial vectors at the two ends).
 // The input is read once; only survivors and the count are written.
+#include <algorithm>
+
 #include "gc_device.cuh"
 #include "gc_internal.h"
 #include "gc_launch.cuh"
@@ -77,13 +79,45 @@ select_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, uint3
     store_run<THREADS, VEC>(out, out_base, s_buf, shift, kept);
 }
 
-// Comparison path ("compaction.cu -- Day 33", compactAtomic): one counter
-// for the whole grid, no scan across tiles, no order between tiles.  Each
-// CTA ranks its tile's survivors (as select_kernel does), claims a run of
-// that many output slots with one atomicAdd on the shared counter, and
-// writes its survivors there; which CTA reaches the counter first decides
-// where its run lands.  One atomic per 4096-element tile instead of one per
-// survivor: the page's version serialises every survivor on one address.
+// The comparison path as "compaction.cu -- Day 33" writes it (compactAtomic):
+// one pass over the input, and every survivor takes its output slot with one
+// atomicAdd on the single counter the whole grid shares, then writes itself
+// there.  No scan and no order: where a survivor lands depends on the order
+// in which the atomics resolve.  The counter is cleared on the stream before
+// the launch (the page's zeroCount).  The grid is a fixed number of CTAs per
+// SM that stride over the input, 16 bytes per thread per step, so the loads
+// stay coalesced; the stores are single elements at whatever slots the
+// atomics return.
+template <class Pred, bool VEC>
+__global__ void __launch_bounds__(256)
+select_atomic_elem_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out,
+                          uint32_t *count, uint32_t n, Pred pred)
+{
+    const uint32_t stride = gridDim.x * blockDim.x;
+    const uint32_t first = blockIdx.x * blockDim.x + threadIdx.x;
+    uint32_t tail = 0u;  // elements before this index went through the vector loop
+    if (VEC) {
+        const uint32_t nvec = n >> 2;
+        for (uint32_t v = first; v < nvec; v += stride) {
+            const uint4 q = __ldcs(reinterpret_cast<const uint4 *>(in) + v);
+            const uint32_t x[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (pred(x[k])) out[atomicAdd(count, 1u)] = x[k];
+        }
+        tail = nvec << 2;
+    }
+    for (uint32_t i = tail + first; i < n; i += stride) {
+        const uint32_t x = __ldcs(in + i);
+        if (pred(x)) out[atomicAdd(count, 1u)] = x;
+    }
+}
+
+// The same comparison with one atomic per tile instead of one per survivor:
+// each CTA ranks its tile's survivors (as select_kernel does), claims a run
+// of that many output slots with one atomicAdd on the shared counter, and
+// writes its survivors there as one contiguous run; which CTA reaches the
+// counter first decides where its run lands.
 template <class Pred, int THREADS, int ROWS, bool VEC>
 __global__ void __launch_bounds__(THREADS)
 select_atomic_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out,
@@ -162,8 +196,8 @@ cudaError_t dispatch_select(const uint32_t *in, uint32_t *out, uint32_t *count, 
 }
 
 template <class Pred>
-cudaError_t dispatch_atomic(const uint32_t *in, uint32_t *out, uint32_t *count, uint32_t n,
-                            Pred pred, cudaStream_t s)
+cudaError_t dispatch_atomic_tile(const uint32_t *in, uint32_t *out, uint32_t *count, uint32_t n,
+                                 Pred pred, cudaStream_t s)
 {
     constexpr int T = gch::kAtomicThreads, R = gch::kAtomicRows;
     const uint32_t tiles = uint32_t(gch::ceil_div(n, gch::tile_elems(T, R)));
@@ -174,6 +208,32 @@ cudaError_t dispatch_atomic(const uint32_t *in, uint32_t *out, uint32_t *count, 
     else
         select_atomic_kernel<Pred, T, R, false><<<tiles, T, 0, s>>>(in, out, count, n, pred);
     return cudaGetLastError();
+}
+
+template <class Pred>
+cudaError_t dispatch_atomic_elem(const uint32_t *in, uint32_t *out, uint32_t *count, uint32_t n,
+                                 Pred pred, cudaStream_t s)
+{
+    constexpr int T = 256;
+    // Enough CTAs to keep every SM's loads in flight; each thread then
+    // strides over the input.
+    const uint32_t want = uint32_t(gch::sm_count()) * 8u;
+    const uint32_t grid = uint32_t(std::max<size_t>(1, std::min<size_t>(want, gch::ceil_div(n, 4 * T))));
+    cudaError_t e = cudaMemsetAsync(count, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return e;
+    if (gch::aligned16(in))
+        select_atomic_elem_kernel<Pred, true><<<grid, T, 0, s>>>(in, out, count, n, pred);
+    else
+        select_atomic_elem_kernel<Pred, false><<<grid, T, 0, s>>>(in, out, count, n, pred);
+    return cudaGetLastError();
+}
+
+template <class Pred>
+cudaError_t dispatch_atomic(const uint32_t *in, uint32_t *out, uint32_t *count, uint32_t n,
+                            Pred pred, cudaStream_t s, bool per_tile)
+{
+    return per_tile ? dispatch_atomic_tile(in, out, count, n, pred, s)
+                    : dispatch_atomic_elem(in, out, count, n, pred, s);
 }
 
 }  // namespace
@@ -210,16 +270,16 @@ cudaError_t launch_select_cmp(const void *in, void *out, uint32_t *count, uint32
 }
 
 cudaError_t launch_select_atomic(const void *in, void *out, uint32_t *count, uint32_t n,
-                                 gc_dtype dt, gc_pred p, cudaStream_t s)
+                                 gc_dtype dt, gc_pred p, cudaStream_t s, bool per_tile)
 {
     auto *i = static_cast<const uint32_t *>(in);
     auto *u = static_cast<uint32_t *>(out);
     switch (p) {
     case GC_PRED_NONZERO:
-        if (dt == GC_F32) return dispatch_atomic(i, u, count, n, gcd::PredNonzeroF32{}, s);
-        return dispatch_atomic(i, u, count, n, gcd::PredNonzeroInt{}, s);
-    case GC_PRED_ODD: return dispatch_atomic(i, u, count, n, gcd::PredOdd{}, s);
-    default: return dispatch_atomic(i, u, count, n, gcd::PredEven{}, s);
+        if (dt == GC_F32) return dispatch_atomic(i, u, count, n, gcd::PredNonzeroF32{}, s, per_tile);
+        return dispatch_atomic(i, u, count, n, gcd::PredNonzeroInt{}, s, per_tile);
+    case GC_PRED_ODD: return dispatch_atomic(i, u, count, n, gcd::PredOdd{}, s, per_tile);
+    default: return dispatch_atomic(i, u, count, n, gcd::PredEven{}, s, per_tile);
     }
 }
 

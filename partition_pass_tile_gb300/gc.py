@@ -71,6 +71,7 @@ def load(path: str | Path | None = None) -> ctypes.CDLL:
         "gc_partition": ([V, V, V, Z, I, I, V, Z, V], S),
         "gc_split_radix": ([V, V, V, V, Z, I, I, V, Z, V], S),
         "gc_select_if_atomic": ([V, V, V, Z, I, I, V, Z, V], S),
+        "gc_select_if_atomic_tile": ([V, V, V, Z, I, I, V, Z, V], S),
         "gc_query_device_status": ([V, V], S),
         "gc_testing_select_if_skip_tile0": ([V, V, V, Z, I, I, V, Z, U64, V], S),
         "gc_testing_exclusive_scan_stalled_barrier": ([V, V, V, Z, I, V, Z, U64, V], S),
@@ -235,7 +236,10 @@ def select_if(x: torch.Tensor, pred, out: torch.Tensor | None = None,
 
 def select_if_atomic(x: torch.Tensor, pred, out: torch.Tensor | None = None,
                      count: torch.Tensor | None = None, ws: torch.Tensor | None = None,
-                     stream=None):
+                     stream=None, per_tile: bool = False):
+    """The atomic-counter comparison path -> (out, count): the survivors in an
+    order the atomics decide.  One atomic per survivor (gc_select_if_atomic),
+    or per tile with per_tile=True (gc_select_if_atomic_tile)."""
     n = x.numel()
     dt = dtype_code(x)
     if out is None:
@@ -243,9 +247,9 @@ def select_if_atomic(x: torch.Tensor, pred, out: torch.Tensor | None = None,
     if count is None:
         count = torch.empty(1, dtype=torch.uint32, device=x.device)
     ws = _ws(ws, OP_SELECT_IF_ATOMIC, n, dt, x.device)
-    _check(load().gc_select_if_atomic(_ptr(x), _ptr(out), _ptr(count), n, dt, pred_code(pred),
-                                      _ptr(ws), ws.numel(), _stream(stream)),
-           "gc_select_if_atomic")
+    name = "gc_select_if_atomic_tile" if per_tile else "gc_select_if_atomic"
+    _check(getattr(load(), name)(_ptr(x), _ptr(out), _ptr(count), n, dt, pred_code(pred),
+                                 _ptr(ws), ws.numel(), _stream(stream)), name)
     return out, count
 
 

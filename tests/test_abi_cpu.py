@@ -35,7 +35,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for want in ["gc_exclusive_scan", "gc_select_if", "gc_partition", "gc_split_radix",
-                 "gc_select_if_atomic", "gc_workspace_bytes", "gc_query_device_status",
+                 "gc_select_if_atomic", "gc_select_if_atomic_tile", "gc_workspace_bytes", "gc_query_device_status",
                  "gc_status_string", "gc_workspace_init", "gc_tile_elements",
                  "gc_testing_select_if_skip_tile0", "gc_inclusive_scan", "gc_select_if_pred",
                  "gc_partition_pred", "gc_select_if_noalloc", "gc_radix_sort",
@@ -88,7 +88,8 @@ def sel(lib, *, i=IN, o=OUT, c=CNT, n=1000, dt=gc.I32, p=gc.NONZERO, ws=WS, wsb=
     return getattr(lib, fn)(i, o, c, n, dt, p, ws, wsb, None)
 
 
-@pytest.mark.parametrize("fn", ["gc_select_if", "gc_select_if_atomic", "gc_partition"])
+@pytest.mark.parametrize("fn", ["gc_select_if", "gc_select_if_atomic", "gc_select_if_atomic_tile",
+                                "gc_partition"])
 def test_select_like_validation(lib, fn):
     E = {v: k for k, v in gc.STATUS.items()}
     assert sel(lib, fn=fn, n=2 ** 31) == E["GC_ERR_INVALID_VALUE"]

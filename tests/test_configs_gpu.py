@@ -33,13 +33,17 @@ def check_select(orc, x, pred, atomic=True):
     assert m == want.shape[0]
     assert np.array_equal(host(out)[:m].view(np.uint32), want.view(np.uint32))
     if atomic:
-        out, cnt = gc.select_if_atomic(xd, pred)
-        m2 = int(host(cnt)[0])
-        got = host(out)[:m2].view(np.uint32)
-        assert m2 == m
-        # the comparator decides its own order: same multiset, order reported only
-        assert np.array_equal(np.sort(got), np.sort(want.view(np.uint32)))
-        return orc.count_out_of_order(got, want.view(np.uint32))
+        # one atomic per survivor (the page's comparator), then one per tile
+        misplaced = []
+        for per_tile in (False, True):
+            out, cnt = gc.select_if_atomic(xd, pred, per_tile=per_tile)
+            m2 = int(host(cnt)[0])
+            got = host(out)[:m2].view(np.uint32)
+            assert m2 == m
+            # the comparator decides its own order: same multiset, order reported only
+            assert np.array_equal(np.sort(got), np.sort(want.view(np.uint32)))
+            misplaced.append(orc.count_out_of_order(got, want.view(np.uint32)))
+        return misplaced
     return None
 
 
@@ -114,6 +118,17 @@ def test_config4_select_sweep(orc, p, seed):
     kept = float((x != 0).mean())
     assert abs(kept - p) < 0.001
     check_select(orc, x, O.NONZERO, atomic=False)
+    # both atomic comparators over the sweep: count and multiset (sorted on
+    # the device, a library sort used only to compare)
+    want = orc.select_if(x, O.NONZERO)
+    want_sorted = torch.sort(to_dev(want.view(np.uint32)).view(torch.int32))[0]
+    xd = to_dev(x)
+    for per_tile in (False, True):
+        out, cnt = gc.select_if_atomic(xd, "nonzero", per_tile=per_tile)
+        m = int(host(cnt)[0])
+        assert m == want.shape[0]
+        got_sorted = torch.sort(out[:m])[0]
+        assert torch.equal(got_sorted, want_sorted)
 
 
 def test_config4_scans_at_roofline_size(orc, big_uniform):

@@ -203,16 +203,23 @@ def test_radix_degenerate(orc):
 
 # ---------------------------------------------------------------- atomic comparator
 
+@pytest.mark.parametrize("per_tile", [False, True], ids=["per_survivor", "per_tile"])
 @pytest.mark.parametrize("dt,pred", CASES)
-def test_atomic_multiset(orc, dt, pred):
-    for n in [1, 33, 4097, 100_003]:
-        x = select_input(n, dt)
-        want = orc.select_if(x, pred)
-        out, cnt = gc.select_if_atomic(dev(x), pred)
-        m = int(host(cnt)[0])
-        got = host(out)[:m]
-        assert m == want.shape[0]
-        assert np.array_equal(np.sort(got.view(np.uint32)), np.sort(want.view(np.uint32)))
+def test_atomic_multiset(orc, dt, pred, per_tile):
+    # several correct answers: the count and the multiset are unique, the order is not
+    for n in [1, 3, 33, 4097, 100_003]:
+        for off in (0, 1):
+            x = select_input(n, dt)
+            want = orc.select_if(x, pred)
+            out = empty_like_offset(dev(x), off, fill=-1)
+            cnt = torch.full((1,), 12345, dtype=torch.int32, device="cuda").view(torch.uint32)
+            gc.select_if_atomic(dev(x, off), pred, out=out, count=cnt, per_tile=per_tile)
+            m = int(host(cnt)[0])
+            got = host(out)
+            assert m == want.shape[0]
+            assert np.array_equal(np.sort(got[:m].view(np.uint32)), np.sort(want.view(np.uint32)))
+            sentinel = host(empty_like_offset(dev(x[:1]), 0, fill=-1))[0]
+            assert np.all(got[m:] == sentinel)  # nothing written past the survivors
 
 
 # ---------------------------------------------------------------- workspace reuse
