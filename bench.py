@@ -12,7 +12,9 @@ sweep workload, 1 GiB per int32 array):
     select_p99    stable select-if NONZERO, 99 % kept
     partition     stable partition, EVEN first (count pre-pass + one pass)
     radix32       LSD radix sort, 32 one-bit splits, uint32 keys + uint32 index payload
-    atomic_p50    atomic-counter select-if (the unordered comparison path), 50 % kept
+    atomic_tile_p50  atomic-counter select-if with one atomic per tile (the unordered
+                  comparison path), 50 % kept; the page's one-atomic-per-survivor form is
+                  timed beside the stable select at 1/50/99 % in the line's `comparator`
 
 Every call goes through the C ABI (libgc.so) via partition_pass_tile_gb300.gc.
 Inputs are 1 GiB each, larger than the 129 MB L2, so no L2 flush is needed
@@ -53,9 +55,9 @@ def workload_name(n: int) -> str:
             "with exclusive scan (int32, float32), 32-bit one-bit-split LSD radix sort "
             "(uint32 keys + index payload) and the atomic select comparator on the same batch")
 OPS = ["scan_i32", "scan_f32", "select_p01", "select_p50", "select_p99", "partition",
-       "radix32", "atomic_p50"]
+       "radix32", "atomic_tile_p50"]
 LAUNCHES_PER_OP = {"scan_i32": 1, "scan_f32": 1, "select_p01": 1, "select_p50": 1,
-                   "select_p99": 1, "partition": 2, "radix32": 33, "atomic_p50": 1}
+                   "select_p99": 1, "partition": 2, "radix32": 33, "atomic_tile_p50": 1}
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, NVIDIA's nominal figure: a secondary denominator
 
@@ -266,7 +268,7 @@ def oracle_step(orc, h: dict, n: int) -> dict:
         ("select_p99", lambda: orc.select_if(h["s99"][:n], O.NONZERO)),
         ("partition", lambda: orc.partition(x, O.EVEN)),
         ("radix32", lambda: orc.split_radix(x.view(np.uint32), h["payload"][:n])),
-        ("atomic_p50", lambda: orc.select_if(h["s50"][:n], O.NONZERO)),
+        ("atomic_tile_p50", lambda: orc.select_if(h["s50"][:n], O.NONZERO)),
     ]
     for name, fn in calls:
         t0 = time.perf_counter()
@@ -367,7 +369,7 @@ def run_gc(args):
             ("partition", lambda: gc.partition(d["x"], "even", out=out_a, count_true=counts[5:6], ws=ws, stream=stream)),
             ("radix32", lambda: gc.split_radix(xk, d["payload"], 0, 32, keys_out=out_a.view(torch.uint32),
                                                vals_out=out_b.view(torch.uint32), ws=ws, stream=stream)),
-            ("atomic_p50", lambda: gc.select_if_atomic(d["s50"], "nonzero", out=out_a, count=counts[7:8], ws=ws, stream=stream)),
+            ("atomic_tile_p50", lambda: gc.select_if_atomic(d["s50"], "nonzero", out=out_a, count=counts[7:8], ws=ws, stream=stream, per_tile=True)),
         ]
         return calls
 
@@ -385,11 +387,11 @@ def run_gc(args):
     stream.synchronize()
     kept_h = counts.view(torch.int32).cpu().numpy().view(np.uint32)
     kept = {"select_p01": int(kept_h[2]), "select_p50": int(kept_h[3]),
-            "select_p99": int(kept_h[4]), "atomic_p50": int(kept_h[7])}
+            "select_p99": int(kept_h[4]), "atomic_tile_p50": int(kept_h[7])}
     # the counts must be the true counts of the inputs (cheap host check)
     for k, key in (("select_p01", "s01"), ("select_p50", "s50"), ("select_p99", "s99")):
         assert kept[k] == int(np.count_nonzero(h[key])), k
-    assert kept["atomic_p50"] == kept["select_p50"]
+    assert kept["atomic_tile_p50"] == kept["select_p50"]
     assert int(kept_h[5]) == int(np.count_nonzero((h["x"] & 1) == 0))
 
     # timed region: every event recorded on the launching stream, read after
@@ -505,7 +507,7 @@ def run_gc(args):
     s_d2h = torch.cuda.Stream(device=dev)
     inputs_of = {"scan_i32": ["x"], "scan_f32": ["f"], "select_p01": ["s01"],
                  "select_p50": ["s50"], "select_p99": ["s99"], "partition": ["x"],
-                 "radix32": ["x", "payload"], "atomic_p50": ["s50"]}
+                 "radix32": ["x", "payload"], "atomic_tile_p50": ["s50"]}
     set_free = [None, None]  # event: the compute stream is done with an input set
     out_free = {name: None for name in OPS}  # event: an op's output has been copied back
 
@@ -521,7 +523,7 @@ def run_gc(args):
             "partition": lambda: gc.partition(dd["x"], "even", out=o["partition"], count_true=counts[5:6], ws=ws, stream=stream),
             "radix32": lambda: gc.split_radix(xk, dd["payload"], 0, 32, keys_out=o["radix32"].view(torch.uint32),
                                               vals_out=out_vals.view(torch.uint32), ws=ws, stream=stream),
-            "atomic_p50": lambda: gc.select_if_atomic(dd["s50"], "nonzero", out=o["atomic_p50"], count=counts[7:8], ws=ws, stream=stream),
+            "atomic_tile_p50": lambda: gc.select_if_atomic(dd["s50"], "nonzero", out=o["atomic_tile_p50"], count=counts[7:8], ws=ws, stream=stream, per_tile=True),
         }
 
     def e2e_step(k):
@@ -579,7 +581,7 @@ def run_gc(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
     # the copied-back counts are the true ones (the step really ran)
     hc = host_counts.numpy().view(np.uint32)
-    assert int(hc[3]) == kept["select_p50"] and int(hc[7]) == kept["atomic_p50"]
+    assert int(hc[3]) == kept["select_p50"] and int(hc[7]) == kept["atomic_tile_p50"]
 
     peak, peak_kind = read_peaks()
     elems_step = len(OPS) * n
@@ -591,6 +593,10 @@ def run_gc(args):
                          "alg_gbs": round(b / op_ms[k] / 1e6, 1),
                          "frac_of_peak": round(b / op_ms[k] / 1e6 / peak, 4),
                          "launches": LAUNCHES_PER_OP[k]}
+    # partition also reads its input in the count pre-pass: 12 B/element moved
+    moved = 12.0 * n + 4
+    ops_report["partition"]["moved_gbs"] = round(moved / op_ms["partition"] / 1e6, 1)
+    ops_report["partition"]["frac_of_peak_moved"] = round(moved / op_ms["partition"] / 1e6 / peak, 4)
     # dominant kernel: the one-bit split of the radix sort (32 launches per sort)
     split_bytes = 16.0 * n
     split_ms = op_ms["radix32"] / 32.0
@@ -795,10 +801,12 @@ def run_configs(args):
         select_row("3 keep odd", x, "odd", "select ODD")
         xd = to_dev(x)
         out = torch.empty_like(xd)
-        ms = gpu_ms(lambda: gc.select_if_atomic(xd, "odd", out=out, count=cnt[1:2], ws=ws, stream=stream), n=n)
         kept = int(np.count_nonzero(x & 1))
-        row("3 keep odd", n, "atomic comparator ODD (multiset)", ms, 4.0 * n + 4.0 * kept + 4,
-            cpu_ms(lambda: orc.select_if(x, oracle.ODD), n), "oracle: the ordered select")
+        for per_tile, label in ((False, "one atomic per survivor"), (True, "one atomic per tile")):
+            ms = gpu_ms(lambda: gc.select_if_atomic(xd, "odd", out=out, count=cnt[1:2], ws=ws, stream=stream,
+                                                    per_tile=per_tile), n=n)
+            row("3 keep odd", n, f"atomic comparator ODD, {label} (multiset)", ms, 4.0 * n + 4.0 * kept + 4,
+                cpu_ms(lambda: orc.select_if(x, oracle.ODD), n), "oracle: the ordered select")
         del xd, out
     n = synth.SIZES["partition"]
     x = synth.uniform_i32(n, synth.SEEDS["partition"])
@@ -826,6 +834,86 @@ def run_configs(args):
         scan_row("roofline", synth.uniform_i32(n, synth.SEEDS["partition"]), "exclusive scan int32")
         scan_row("roofline", synth.scan_unit_f32(n, synth.SEEDS["scan_f32"]), "exclusive scan float32")
         select_row("roofline", synth.keep_fraction(n, 0.5, 42), "nonzero", "select NONZERO p=0.5")
+        select_row("roofline", synth.keep_fraction(n, 0.01, 41), "nonzero", "select NONZERO p=0.01")
+
+    # Pointers 4-byte but not 16-byte aligned: the one-tile-per-CTA kernels
+    # (dynamic tile ids, warp look-back, register tiles), at 2^26.
+    n = 1 << 26
+    for name, a, op in (("exclusive scan int32", synth.uniform_i32(n, 4), "scan"),
+                        ("select NONZERO p=0.5", synth.keep_fraction(n, 0.5, 42), "select"),
+                        ("partition EVEN", synth.uniform_i32(n, 4), "partition")):
+        big = torch.zeros(n + 1, dtype=torch.int32)
+        big[1:] = torch.from_numpy(a)
+        xd = big.to(dev)[1:]
+        ob = torch.empty(n + 1, dtype=torch.int32, device=dev)
+        out = ob[1:]
+        if op == "scan":
+            ms = gpu_ms(lambda: gc.exclusive_scan(xd, out=out, total=cnt[0:1].view(torch.int32), ws=ws, stream=stream), n=n)
+            nbytes, oms = 8.0 * n, cpu_ms(lambda: orc.exclusive_scan(a), n)
+        elif op == "select":
+            kept = int(np.count_nonzero(a))
+            ms = gpu_ms(lambda: gc.select_if(xd, "nonzero", out=out, count=cnt[0:1], ws=ws, stream=stream), n=n)
+            nbytes, oms = 4.0 * n + 4.0 * kept + 4, cpu_ms(lambda: orc.select_if(a, oracle.NONZERO), n)
+        else:
+            ms = gpu_ms(lambda: gc.partition(xd, "even", out=out, count_true=cnt[0:1], ws=ws, stream=stream), n=n)
+            nbytes, oms = 8.0 * n, cpu_ms(lambda: orc.partition(a, oracle.EVEN), n)
+        row("misaligned (4-byte) pointers", n, name, ms, nbytes, oms,
+            "input and output one element into their allocations: the one-tile-per-CTA kernels")
+        del xd, ob, out
+
+    # The sharded path on one GPU: P = 4 shards of the 2^28 array, each a
+    # pre-pass, the offsets of its shard and the placed pass; the whole
+    # sequence timed.  Algorithmic bytes are the whole array's; the pre-pass
+    # reads every element once more.
+    from partition_pass_tile_gb300 import shard
+    n, P = 1 << 28, 4
+    bounds = [shard.shard_bounds(n, P, r) for r in range(P)]
+    sizes = [b - a for a, b in bounds]
+    totals = torch.empty(P, dtype=torch.uint32, device=dev)
+    itot = totals.view(torch.int32)
+    offs = torch.empty((P, 2), dtype=torch.int64, device=dev)
+    carries = torch.empty(P, dtype=torch.int32, device=dev)
+    x = synth.uniform_i32(n, synth.SEEDS["partition"])
+    xd = to_dev(x)
+    out = torch.empty_like(xd)
+
+    def sharded_scan():
+        for r, (a, b) in enumerate(bounds):
+            gc.reduce(xd[a:b], total=itot[r:r + 1], ws=ws, stream=stream)
+        for r, (a, b) in enumerate(bounds):
+            gc.shard_offsets(gc.OP_EXCLUSIVE_SCAN, itot, r, out=carries[r:r + 1], stream=stream)
+            gc.exclusive_scan_carry(xd[a:b], carries[r:r + 1], out=out[a:b], with_total=False, ws=ws,
+                                    stream=stream)
+
+    def sharded_partition():
+        for r, (a, b) in enumerate(bounds):
+            gc.count_if(xd[a:b], "even", count=totals[r:r + 1], ws=ws, stream=stream)
+        for r, (a, b) in enumerate(bounds):
+            gc.shard_offsets(gc.OP_PARTITION, totals, r, sizes=sizes, dtype=gc.U32, out=offs[r], stream=stream)
+            gc.partition_at(xd[a:b], "even", out, offs[r], count_true=cnt[r:r + 1] if r < 4 else None,
+                            ws=ws, stream=stream)
+    ms = gpu_ms(sharded_scan, reps=5, n=n)
+    row("sharded, 4 shards on one GPU", n, "exclusive scan int32 (reduce + carry-in scan)", ms, 8.0 * n,
+        cpu_ms(lambda: orc.exclusive_scan(x), n), "moves 12 B/element: the pre-pass reads the input once more")
+    ms = gpu_ms(sharded_partition, reps=5, n=n)
+    row("sharded, 4 shards on one GPU", n, "partition EVEN (count + placed pass)", ms, 8.0 * n,
+        cpu_ms(lambda: orc.partition(x, oracle.EVEN), n), "moves 12 B/element, as the one-array partition")
+    del xd, out
+    y = synth.keep_fraction(n, 0.5, 42)
+    yd = to_dev(y)
+    out = torch.empty_like(yd)
+    kept = int(np.count_nonzero(y))
+
+    def sharded_select():
+        for r, (a, b) in enumerate(bounds):
+            gc.count_if(yd[a:b], "nonzero", count=totals[r:r + 1], ws=ws, stream=stream)
+        for r, (a, b) in enumerate(bounds):
+            gc.shard_offsets(gc.OP_SELECT_IF, totals, r, dtype=gc.U32, out=offs[r, :1], stream=stream)
+            gc.select_if_at(yd[a:b], "nonzero", out, offs[r, :1], count=cnt[r:r + 1], ws=ws, stream=stream)
+    ms = gpu_ms(sharded_select, reps=5, n=n)
+    row("sharded, 4 shards on one GPU", n, "select NONZERO p=0.5 (count + placed pass)", ms,
+        4.0 * n + 4.0 * kept + 4, cpu_ms(lambda: orc.select_if(y, oracle.NONZERO), n),
+        "moves 8 + 4 * kept B/element: the pre-pass reads the input once more")
 
 
 def main(argv=None):

@@ -141,7 +141,9 @@ typedef enum {
     GC_OP_SPLIT_RADIX = 3,
     GC_OP_SELECT_IF_ATOMIC = 4,
     GC_OP_INCLUSIVE_SCAN = 5,
-    GC_OP_RADIX_SORT = 6
+    GC_OP_RADIX_SORT = 6,
+    GC_OP_REDUCE = 7,      /* gc_reduce */
+    GC_OP_COUNT_IF = 8     /* gc_count_if */
 } gc_op;
 
 /* Static, never NULL, "unknown status" for values outside the enum. */
@@ -175,8 +177,11 @@ gc_status gc_workspace_init(void *d_ws, size_t ws_bytes, cudaStream_t stream);
  * d_total (nullable) receives in[0] + ... + in[n-1] as one element of dtype.
  * int32 and uint32 add modulo 2^32 (the same bits).  float32 adds within a
  * tile in float32 with round-to-nearest and carries the running prefix
- * between tiles in float64, so the result is within a few float32 ulps of
- * the exact prefix; the summation order is not sequential.
+ * between tiles as an unevaluated pair of float32 values (about 48
+ * significant bits; the kernel for pointers that are not 16-byte aligned
+ * carries a float64), and each output is hi + (lo + the in-tile sum), so the
+ * result is within a few float32 ulps of the exact prefix; the summation
+ * order is not sequential.
  */
 gc_status gc_exclusive_scan(const void *d_in, void *d_out, void *d_total,
                             size_t n, gc_dtype dtype, void *d_ws,
@@ -313,16 +318,128 @@ gc_status gc_select_if_atomic_tile(const void *d_in, void *d_out, uint32_t *d_co
  * make that first call before any stream capture begins.  Every call shares
  * the array: each clears what must start at zero on its own stream, and
  * calls that can overlap on the GPU (different streams with no ordering
- * between them) race on it.  Device-side timeouts of this entry point are
- * recorded in that array, which no query reads; a start-barrier timeout
- * (only possible if the cooperative grid were not all resident) would leave
- * the array's barrier marked, and every later call in the process would then
- * wait out its time limit (1 s) before finishing.  No allocation of any kind.
+ * between them) race on it.  Device-side failures of this entry point (a
+ * bounded wait that gave up, a refused store) are recorded in that array and
+ * reported by gc_select_if_noalloc_status.  The cached address belongs to
+ * the device's primary context: after a cudaDeviceReset the array and the
+ * cache are gone, and the library must not be called again in that process.
+ * No allocation of any kind.
  */
 #define GC_NOALLOC_MAX_ELEMENTS 268435456u
 gc_status gc_select_if_noalloc(const void *d_in, void *d_out, uint32_t *d_count,
                                size_t n, gc_dtype dtype, gc_pred pred,
                                cudaStream_t stream);
+
+/*
+ * SYNCHRONOUS.  gc_query_device_status for the fixed array of
+ * gc_select_if_noalloc on the current device: waits for `stream`, reads and
+ * clears the array's error word, and after an error also resets its start
+ * barrier, which a barrier wait that gave up leaves marked (so that later
+ * calls time out instead of passing it early).  Returns GC_OK,
+ * GC_ERR_TIMEOUT or GC_ERR_DEVICE_CHECK (the outputs of the failed call are
+ * undefined), or GC_ERR_CUDA.  Like the entry point it allocates nothing.
+ */
+gc_status gc_select_if_noalloc_status(cudaStream_t stream);
+
+/*
+ * ---------------------------------------------------------------- shards
+ *
+ * A scan, select-if or partition of one array cut into P contiguous shards
+ * (one per GPU, each in its own memory, or several on one GPU), computed
+ * shard by shard.  Each shard needs only what the shards before it
+ * contribute: the sum of their elements (scan), the number of survivors
+ * before it (select-if), and for partition also the total number kept, T,
+ * since rejected elements start at T.  That is the decoupled look-back of
+ * "The CUDA Handbook, ch. 13: Stream compaction" one level up, tiles
+ * becoming shards, and the kept / rejected addressing rank[i] and
+ * T + i - rank[i] of "compaction.cu -- Day 33" (scatterPartition).
+ *
+ * Sequence on rank r, all on one stream, nothing read back to the host:
+ *   1. pre-pass: gc_reduce (scan) or gc_count_if (select-if, partition)
+ *      writes this shard's total into slot r of a device array of P words;
+ *   2. exchange: every rank gathers the P words (an all-gather, e.g. NCCL;
+ *      on one GPU the P slots are simply written in place);
+ *   3. gc_shard_offsets computes rank r's offsets from the P words;
+ *   4. the placed pass: gc_exclusive_scan_carry, gc_select_if_at or
+ *      gc_partition_at.
+ * Every placed pass reads the input once more (4 B per element), so a
+ * sharded scan moves 12 B per element and a sharded select-if 8 + 4 * kept.
+ */
+#define GC_MAX_SHARDS 65536u
+
+/*
+ * d_total (one element of dtype) = in[0] + ... + in[n-1]: int32 / uint32
+ * modulo 2^32, float32 summed in float pairs per thread and in double across
+ * CTAs, rounded once (deterministic for a given device).  Workspace:
+ * gc_workspace_bytes(GC_OP_REDUCE, n, dtype).  n == 0 writes 0.
+ */
+gc_status gc_reduce(const void *d_in, void *d_total, size_t n, gc_dtype dtype, void *d_ws,
+                    size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * *d_count = how many of the n elements pred keeps (the count pre-pass of
+ * gc_partition alone).  Workspace: gc_workspace_bytes(GC_OP_COUNT_IF, ...).
+ * Errors as gc_select_if.
+ */
+gc_status gc_count_if(const void *d_in, uint32_t *d_count, size_t n, gc_dtype dtype,
+                      gc_pred pred, void *d_ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Offsets of shard `rank` of `parts` (device writes, one thread):
+ *   op GC_OP_EXCLUSIVE_SCAN: d_totals = parts elements of dtype (the shards'
+ *       gc_reduce totals); d_offsets receives one element of dtype, the sum
+ *       of totals [0, rank) (int modulo 2^32; float32 summed in double).
+ *   op GC_OP_SELECT_IF: d_totals = parts uint32 counts; d_offsets receives
+ *       one uint64 (8-byte aligned), the sum of counts [0, rank).
+ *   op GC_OP_PARTITION: as select-if, plus h_sizes (host, parts element
+ *       counts, read during the call); d_offsets receives two uint64: kept
+ *       before = counts [0, rank) summed, and the first rejected position
+ *       T + (h_sizes [0, rank) summed) - kept before, T = all counts summed.
+ * h_sizes is ignored except for partition.  Errors: GC_ERR_INVALID_VALUE for
+ * another op, a bad dtype, parts == 0 or > GC_MAX_SHARDS, rank >= parts,
+ * NULL pointers or a size > GC_MAX_ELEMENTS; GC_ERR_MISALIGNED.
+ */
+gc_status gc_shard_offsets(gc_op op, gc_dtype dtype, const uint32_t *d_totals,
+                           const uint64_t *h_sizes, size_t parts, size_t rank, void *d_offsets,
+                           cudaStream_t stream);
+
+/*
+ * gc_exclusive_scan plus a carry-in: out[i] = *d_carry + in[0] + ... +
+ * in[i-1], and d_total (nullable) = *d_carry + the sum of all n, i.e. the
+ * carry of the shard after this one.  d_carry is one device element of
+ * dtype, read by the kernel (non-NULL).  Same workspace, precision, in-place
+ * rule and errors as gc_exclusive_scan; n == 0 copies the carry to d_total.
+ */
+gc_status gc_exclusive_scan_carry(const void *d_in, void *d_out, void *d_total, size_t n,
+                                  gc_dtype dtype, const void *d_carry, void *d_ws,
+                                  size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * gc_select_if whose survivors go to d_out[*d_base + rank] instead of
+ * d_out[rank]: d_out is the whole output (out_capacity elements, in this
+ * device's memory) and *d_base (device uint64, 8-byte aligned) the number
+ * of survivors of the shards before this one.  *d_count receives this
+ * shard's own count.  A run that would end past out_capacity is not written
+ * and is reported as GC_ERR_DEVICE_CHECK by gc_query_device_status.
+ * Workspace and errors as gc_select_if.
+ */
+gc_status gc_select_if_at(const void *d_in, void *d_out, size_t out_capacity,
+                          const uint64_t *d_base, uint32_t *d_count, size_t n, gc_dtype dtype,
+                          gc_pred pred, void *d_ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * gc_partition of one shard into the whole output: kept elements to
+ * d_out[d_offsets[0] + rank[i]], rejected ones to d_out[d_offsets[1] + i -
+ * rank[i]] (the two uint64 of gc_shard_offsets), so that the shards together
+ * write the stable partition of the whole array.  One pass, no count
+ * pre-pass (T is in the offsets).  *d_count_true receives this shard's kept
+ * count.  out_capacity >= n; runs past it are refused as in gc_select_if_at.
+ * Workspace and errors as gc_partition.
+ */
+gc_status gc_partition_at(const void *d_in, void *d_out, size_t out_capacity,
+                          const uint64_t *d_offsets, uint32_t *d_count_true, size_t n,
+                          gc_dtype dtype, gc_pred pred, void *d_ws, size_t ws_bytes,
+                          cudaStream_t stream);
 
 /*
  * SYNCHRONOUS.  Waits for `stream`, then reads and clears the device-side

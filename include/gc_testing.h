@@ -47,6 +47,21 @@ gc_status gc_testing_exclusive_scan_stalled_barrier(const void *d_in, void *d_ou
                                                     size_t ws_bytes, uint64_t timeout_ns,
                                                     cudaStream_t stream);
 
+/*
+ * gc_select_if_noalloc with a stalled start barrier: the fixed array's
+ * arrival counter is marked as a barrier wait that ran out leaves it, so
+ * every CTA's barrier wait gives up after timeout_ns, records GC_ERR_TIMEOUT
+ * and carries on.  Requires a 16-byte-aligned d_in and n >= 1 (otherwise
+ * GC_ERR_INVALID_VALUE), else the argument errors of gc_select_if_noalloc.
+ * The output is undefined; gc_select_if_noalloc_status then returns
+ * GC_ERR_TIMEOUT and clears the barrier.
+ */
+gc_status gc_testing_select_if_noalloc_stalled_barrier(const void *d_in, void *d_out,
+                                                       uint32_t *d_count, size_t n,
+                                                       gc_dtype dtype, gc_pred pred,
+                                                       uint64_t timeout_ns,
+                                                       cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

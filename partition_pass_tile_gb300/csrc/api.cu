@@ -218,6 +218,10 @@ size_t gc_workspace_bytes(gc_op op, size_t n, gc_dtype dtype)
     case GC_OP_RADIX_SORT:
         if (!valid_dtype(dtype)) return 0;
         return digit_table_offset(n) + digit_table_bytes(n);
+    case GC_OP_REDUCE:
+    case GC_OP_COUNT_IF:
+        if (!valid_dtype(dtype)) return 0;
+        return kHeaderBytes + status;
     case GC_OP_SPLIT_RADIX:
         return radix_temp_offset(n) + 2 * radix_temp_stride(n);
     }
@@ -234,6 +238,8 @@ size_t gc_tile_elements(gc_op op)
     case GC_OP_SPLIT_RADIX: return split_tile_elems();
     case GC_OP_RADIX_SORT: return kDigitTile;
     case GC_OP_SELECT_IF_ATOMIC: return atomic_tile_elems();
+    case GC_OP_REDUCE:
+    case GC_OP_COUNT_IF: return 4 * kReduceThreads;
     }
     return 0;
 }
@@ -437,6 +443,134 @@ gc_status gc_radix_sort(const void *d_keys_in, const uint32_t *d_vals_in, void *
                                               static_cast<uint32_t *>(d_keys_out), d_vals_out,
                                               uint32_t(n), neg, flip, static_cast<uint8_t *>(d_ws),
                                               stream, LaunchOpts{}));
+}
+
+// ---------------------------------------------------------------- sharded calls
+
+gc_status gc_reduce(const void *d_in, void *d_total, size_t n, gc_dtype dtype, void *d_ws,
+                    size_t ws_bytes, cudaStream_t stream)
+{
+    gc_status st = check_common(d_in, d_in, n, d_ws, ws_bytes, GC_OP_REDUCE, dtype);
+    if (st != GC_OK) return st;
+    if (d_total == nullptr) return GC_ERR_INVALID_VALUE;
+    if (!aligned4(d_total)) return GC_ERR_MISALIGNED;
+    if (overlap(d_total, 4, d_in, 4 * n) || overlap(d_total, 4, d_ws, ws_bytes))
+        return GC_ERR_INVALID_VALUE;
+    if (n == 0) return from_cuda(cudaMemsetAsync(d_total, 0, 4, stream));
+    return from_cuda(launch_reduce(d_in, d_total, uint32_t(n), dtype, static_cast<uint8_t *>(d_ws),
+                                   stream));
+}
+
+gc_status gc_count_if(const void *d_in, uint32_t *d_count, size_t n, gc_dtype dtype, gc_pred pred,
+                      void *d_ws, size_t ws_bytes, cudaStream_t stream)
+{
+    gc_status st = check_common(d_in, d_in, n, d_ws, ws_bytes, GC_OP_COUNT_IF, dtype);
+    if (st != GC_OK) return st;
+    if (!valid_pred(pred)) return GC_ERR_INVALID_VALUE;
+    if (dtype == GC_F32 && pred != GC_PRED_NONZERO) return GC_ERR_UNSUPPORTED;
+    if (d_count == nullptr) return GC_ERR_INVALID_VALUE;
+    if (!aligned4(d_count)) return GC_ERR_MISALIGNED;
+    if (overlap(d_count, 4, d_in, 4 * n) || overlap(d_count, 4, d_ws, ws_bytes))
+        return GC_ERR_INVALID_VALUE;
+    if (n == 0) return from_cuda(cudaMemsetAsync(d_count, 0, 4, stream));
+    return from_cuda(launch_count_if(d_in, d_count, uint32_t(n), dtype, pred,
+                                     static_cast<uint8_t *>(d_ws), stream));
+}
+
+gc_status gc_exclusive_scan_carry(const void *d_in, void *d_out, void *d_total, size_t n,
+                                  gc_dtype dtype, const void *d_carry, void *d_ws,
+                                  size_t ws_bytes, cudaStream_t stream)
+{
+    if (d_carry == nullptr) return GC_ERR_INVALID_VALUE;
+    if (!aligned4(d_carry)) return GC_ERR_MISALIGNED;
+    gc_status st = check_common(d_in, d_out, n, d_ws, ws_bytes, GC_OP_EXCLUSIVE_SCAN, dtype);
+    if (st != GC_OK) return st;
+    if (n > 0 && d_in != d_out && overlap(d_in, 4 * n, d_out, 4 * n)) return GC_ERR_INVALID_VALUE;
+    if (overlap(d_carry, 4, d_out, 4 * n) || overlap(d_carry, 4, d_ws, ws_bytes))
+        return GC_ERR_INVALID_VALUE;
+    if (d_total != nullptr) {
+        if (!aligned4(d_total)) return GC_ERR_MISALIGNED;
+        if (overlap(d_total, 4, d_out, 4 * n) || overlap(d_total, 4, d_in, 4 * n) ||
+            overlap(d_total, 4, d_ws, ws_bytes) || overlap(d_total, 4, d_carry, 4))
+            return GC_ERR_INVALID_VALUE;
+    }
+    if (n == 0)  // the total of nothing after the carry is the carry
+        return d_total ? from_cuda(cudaMemcpyAsync(d_total, d_carry, 4, cudaMemcpyDeviceToDevice,
+                                                   stream))
+                       : GC_OK;
+    return from_cuda(launch_scan(d_in, d_out, d_total, uint32_t(n), dtype,
+                                 static_cast<uint8_t *>(d_ws), stream, LaunchOpts{}, false,
+                                 d_carry));
+}
+
+gc_status gc_select_if_at(const void *d_in, void *d_out, size_t out_capacity,
+                          const uint64_t *d_base, uint32_t *d_count, size_t n, gc_dtype dtype,
+                          gc_pred pred, void *d_ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (d_base == nullptr) return GC_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(d_base) & 7u) != 0) return GC_ERR_MISALIGNED;
+    gc_status st = check_select_like(d_in, d_out, d_count, n, dtype, pred, d_ws, ws_bytes,
+                                     GC_OP_SELECT_IF);
+    if (st != GC_OK) return st;
+    if (n > 0) {
+        if (out_capacity == 0 || out_capacity > (size_t(1) << 62)) return GC_ERR_INVALID_VALUE;
+        const size_t ob = 4 * out_capacity;
+        if (overlap(d_out, ob, d_in, 4 * n) || overlap(d_out, ob, d_ws, ws_bytes) ||
+            overlap(d_out, ob, d_count, 4) || overlap(d_out, ob, d_base, 8))
+            return GC_ERR_INVALID_VALUE;
+    }
+    if (n == 0) return from_cuda(cudaMemsetAsync(d_count, 0, sizeof(uint32_t), stream));
+    return from_cuda(launch_select(d_in, d_out, d_count, uint32_t(n), dtype, pred,
+                                   static_cast<uint8_t *>(d_ws), stream, LaunchOpts{}, d_base,
+                                   uint64_t(out_capacity)));
+}
+
+gc_status gc_partition_at(const void *d_in, void *d_out, size_t out_capacity,
+                          const uint64_t *d_offsets, uint32_t *d_count_true, size_t n,
+                          gc_dtype dtype, gc_pred pred, void *d_ws, size_t ws_bytes,
+                          cudaStream_t stream)
+{
+    if (d_offsets == nullptr) return GC_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(d_offsets) & 7u) != 0) return GC_ERR_MISALIGNED;
+    gc_status st = check_select_like(d_in, d_out, d_count_true, n, dtype, pred, d_ws, ws_bytes,
+                                     GC_OP_PARTITION);
+    if (st != GC_OK) return st;
+    if (n > 0) {
+        if (out_capacity < n || out_capacity > (size_t(1) << 62)) return GC_ERR_INVALID_VALUE;
+        const size_t ob = 4 * out_capacity;
+        if (overlap(d_out, ob, d_in, 4 * n) || overlap(d_out, ob, d_ws, ws_bytes) ||
+            overlap(d_out, ob, d_count_true, 4) || overlap(d_out, ob, d_offsets, 16))
+            return GC_ERR_INVALID_VALUE;
+    }
+    if (n == 0) return from_cuda(cudaMemsetAsync(d_count_true, 0, sizeof(uint32_t), stream));
+    return from_cuda(launch_partition_at(d_in, d_out, uint64_t(out_capacity), d_offsets,
+                                         d_count_true, uint32_t(n), dtype, pred,
+                                         static_cast<uint8_t *>(d_ws), stream, LaunchOpts{}));
+}
+
+gc_status gc_shard_offsets(gc_op op, gc_dtype dtype, const uint32_t *d_totals,
+                           const uint64_t *h_sizes, size_t parts, size_t rank, void *d_offsets,
+                           cudaStream_t stream)
+{
+    if (op != GC_OP_EXCLUSIVE_SCAN && op != GC_OP_SELECT_IF && op != GC_OP_PARTITION)
+        return GC_ERR_INVALID_VALUE;
+    if (!valid_dtype(dtype)) return GC_ERR_INVALID_VALUE;
+    if (parts == 0 || parts > GC_MAX_SHARDS || rank >= parts) return GC_ERR_INVALID_VALUE;
+    if (d_totals == nullptr || d_offsets == nullptr) return GC_ERR_INVALID_VALUE;
+    if (!aligned4(d_totals)) return GC_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(d_offsets) & (op == GC_OP_EXCLUSIVE_SCAN ? 3u : 7u)) != 0)
+        return GC_ERR_MISALIGNED;
+    uint64_t before = 0;
+    if (op == GC_OP_PARTITION) {
+        if (h_sizes == nullptr) return GC_ERR_INVALID_VALUE;
+        for (size_t q = 0; q < parts; ++q)
+            if (h_sizes[q] > GC_MAX_ELEMENTS) return GC_ERR_INVALID_VALUE;
+        for (size_t q = 0; q < rank; ++q) before += h_sizes[q];
+    }
+    const size_t out_bytes = op == GC_OP_EXCLUSIVE_SCAN ? 4 : (op == GC_OP_PARTITION ? 16 : 8);
+    if (overlap(d_offsets, out_bytes, d_totals, 4 * parts)) return GC_ERR_INVALID_VALUE;
+    return from_cuda(launch_shard_offsets(op, dtype, d_totals, uint32_t(parts), uint32_t(rank),
+                                          before, d_offsets, stream));
 }
 
 gc_status gc_query_device_status(void *d_ws, cudaStream_t stream)

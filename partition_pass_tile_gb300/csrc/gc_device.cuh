@@ -808,7 +808,10 @@ __device__ __forceinline__ uint32_t window_lo(uint32_t k)
 // whole iteration earlier.  The loads of that window are issued before the
 // reduction of tile k and consumed after it, so their latency overlaps the
 // reduction.  kWinPerThread bounds the window: G - 1 <= THREADS * kWinPerThread.
-constexpr int kWinPerThread = 4;
+#ifndef GC_WIN_PER_THREAD
+#define GC_WIN_PER_THREAD 2
+#endif
+constexpr int kWinPerThread = GC_WIN_PER_THREAD;
 
 struct WindowLoads {
     uint64_t w[kWinPerThread];

@@ -157,8 +157,11 @@ cudaError_t reset_tiles(uint8_t *ws, size_t tiles, cudaStream_t s, bool skip_fir
 cudaError_t clear_accumulators(uint8_t *ws, cudaStream_t s);
 
 // Launchers.  All arguments were validated by api.cu; n >= 1.
+// carry (device, nullable): one element of dt added to every output and to
+// the total.
 cudaError_t launch_scan(const void *in, void *out, void *total, uint32_t n, gc_dtype dt,
-                        uint8_t *ws, cudaStream_t s, const LaunchOpts &o, bool inclusive = false);
+                        uint8_t *ws, cudaStream_t s, const LaunchOpts &o, bool inclusive = false,
+                        const void *carry = nullptr);
 
 // A parameterised predicate as the kernels take it (see gcd::PredCmp): keep
 // keys in [lo, lo + span] (xor invert), or (x & mask) == value (xor invert).
@@ -170,8 +173,12 @@ cudaError_t launch_select_cmp(const void *in, void *out, uint32_t *count, uint32
 cudaError_t launch_partition_cmp(const void *in, void *out, uint32_t *count_true, uint32_t n,
                                  gc_dtype dt, const CmpSpec &c, uint8_t *ws, cudaStream_t s,
                                  const LaunchOpts &o);
+// obase (device, nullable): survivors go to out[*obase + rank]; a run that
+// would end past cap (elements of out) is refused on the device
+// (GC_ERR_DEVICE_CHECK).  Without obase, cap is n.
 cudaError_t launch_select(const void *in, void *out, uint32_t *count, uint32_t n, gc_dtype dt,
-                          gc_pred p, uint8_t *ws, cudaStream_t s, const LaunchOpts &o);
+                          gc_pred p, uint8_t *ws, cudaStream_t s, const LaunchOpts &o,
+                          const uint64_t *obase = nullptr, uint64_t cap = 0);
 // per_tile: one atomic per tile (gc_select_if_atomic_tile); otherwise one
 // per survivor (gc_select_if_atomic).
 cudaError_t launch_select_atomic(const void *in, void *out, uint32_t *count, uint32_t n,
@@ -183,6 +190,22 @@ cudaError_t launch_split_radix(const uint32_t *keys_in, const uint32_t *vals_in,
                                uint32_t *keys_out, uint32_t *vals_out, uint32_t n, int begin_bit,
                                int end_bit, uint8_t *ws, cudaStream_t s, const LaunchOpts &o,
                                uint32_t key_neg = 0u, uint32_t key_flip = 0u);
+
+// The pre-passes of a scan, select-if or partition split over shards, and
+// the placed partition.  See gc_reduce, gc_count_if, gc_partition_at.
+cudaError_t launch_reduce(const void *in, void *total, uint32_t n, gc_dtype dt, uint8_t *ws,
+                          cudaStream_t s);
+cudaError_t launch_count_if(const void *in, uint32_t *count, uint32_t n, gc_dtype dt, gc_pred p,
+                            uint8_t *ws, cudaStream_t s);
+cudaError_t launch_partition_at(const void *in, void *out, uint64_t capacity,
+                                const uint64_t *offsets, uint32_t *count_true, uint32_t n,
+                                gc_dtype dt, gc_pred p, uint8_t *ws, cudaStream_t s,
+                                const LaunchOpts &o);
+// One thread: the offsets of shard `rank` from the totals of all `parts`
+// shards (gc_shard_offsets).
+cudaError_t launch_shard_offsets(gc_op op, gc_dtype dt, const uint32_t *totals, uint32_t parts,
+                                 uint32_t rank, uint64_t sizes_before, void *offsets,
+                                 cudaStream_t s);
 
 cudaError_t launch_radix_sort_digits(const uint32_t *keys_in, const uint32_t *vals_in,
                                      uint32_t *keys_out, uint32_t *vals_out, uint32_t n,

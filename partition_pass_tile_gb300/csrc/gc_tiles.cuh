@@ -162,6 +162,7 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
 
     uint32_t run_u = 0u;     // inclusive prefix of the tile before the previous one
     float run_h = 0.0f, run_l = 0.0f;  // the same for float32, as a float pair
+    op.seed(run_u, run_h, run_l);      // a scan's carry-in, where it has one
     uint32_t prev_agg = 0u;  // aggregate bits of the previous tile
     typename Op::Carry cur{}, prv{};  // per-thread results of a reduction kept for its finish
 
@@ -299,10 +300,22 @@ struct ScanOp {
     const uint32_t *srcs[1];
     uint32_t *out;
     uint32_t *total;
+    const uint32_t *carry;  // device, nullable: a value of the dtype added to every output
 
     struct Carry {};
     static constexpr bool kPreload = false;
     struct Loaded {};
+
+    // The running prefix before the first tile: the carry-in, or 0.
+    __device__ __forceinline__ void seed(uint32_t &u, float &h, float &l) const
+    {
+        if (carry != nullptr) {
+            const uint32_t c = *carry;
+            u = c;
+            h = __uint_as_float(c);
+            l = 0.0f;
+        }
+    }
 
     template <bool FULL, class P>
     __device__ __forceinline__ void load(const P &, int, uint32_t, uint32_t, uint32_t, uint32_t,
@@ -469,6 +482,14 @@ __device__ __forceinline__ uint32_t rank_tile(const uint32_t *sbuf, const uint32
     return kept;
 }
 
+// Output placement of a select-if: survivors go to out[obase + rank], and a
+// tile whose run would end past cap records GC_ERR_DEVICE_CHECK and stores
+// nothing (obase = null, read as 0, and cap = n for the plain entry point).
+struct SelectPlacement {
+    const uint64_t *obase;
+    uint64_t cap;
+};
+
 // Stable select-if.  The tile's survivors are compacted in place inside its
 // own stage buffer (every element was read into registers before the barrier
 // that precedes the first write, and a survivor's rank never exceeds its
@@ -486,11 +507,14 @@ struct SelectOp {
     uint32_t *out;
     uint32_t *count;
     Pred pred;
+    SelectPlacement place;
+    uint8_t *ws;  // the error word of a refused run
 
     struct Carry {
         uint32_t mask[ROWS];
         uint32_t base[ROWS];
     };
+    __device__ __forceinline__ void seed(uint32_t &, float &, float &) const {}
     // The tile is read into registers before the window barrier, which then
     // also orders those reads before the in-place compaction's writes.
     static constexpr bool kPreload = true;
@@ -524,27 +548,34 @@ struct SelectOp {
                                            const Loaded &ld) const
     {
         uint32_t *buf = pipe.buf(s);
+        if (threadIdx.x == 0 && last) *count = before + kept;
+        // placed output: out[obase + before + rank], refused past cap
+        const uint64_t ob = place.obase != nullptr ? __ldg(place.obase) : 0ull;
+        if (ob + before + kept > place.cap) {
+            if (threadIdx.x == 0) record_error(ws, kDeviceCheckCode, tile);
+            return;
+        }
+        uint32_t *const o = out + (ob & ~3ull);
+        const uint32_t d0 = uint32_t(ob & 3ull) + before;  // index into o
         if (kept < kSparse) {
             // Survivor q of vector r goes to before + base[r] + (survivors of
             // the vector before it); no shared-memory writes, so no barrier.
 #pragma unroll
             for (int r = 0; r < ROWS; ++r) {
                 uint32_t m = c.mask[r];
-                uint32_t pos = before + c.base[r];
+                uint32_t pos = d0 + c.base[r];
                 const uint32_t li = r * TT::kRowElems + 4 * threadIdx.x;
                 while (m != 0u) {
                     const uint32_t q = uint32_t(__ffs(m) - 1);
                     m &= m - 1u;
                     const uint32_t x = (FULL || li + 4u <= staged) ? buf[li + q] : srcs[0][base + li + q];
-                    __stcs(out + pos, x);
+                    __stcs(o + pos, x);
                     ++pos;
                 }
             }
-            if (threadIdx.x == 0 && last) *count = before + kept;
-            (void)tile;
             return;
         }
-        const uint32_t shift = VEC ? (before & 3u) : 0u;
+        const uint32_t shift = VEC ? (d0 & 3u) : 0u;
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) {
             uint32_t pos = shift + c.base[r];
@@ -555,13 +586,11 @@ struct SelectOp {
         if (VEC && kept >= kBulkMinRun) {
             fence_proxy_async_smem();
             __syncthreads();
-            store_run_bulk<THREADS>(out, before, buf, shift, kept, 0);
+            store_run_bulk<THREADS>(o, d0, buf, shift, kept, 0);
         } else {
             __syncthreads();
-            store_run<THREADS, VEC>(out, before, buf, shift, kept);
+            store_run<THREADS, VEC>(o, d0, buf, shift, kept);
         }
-        if (threadIdx.x == 0 && last) *count = before + kept;
-        (void)tile;
     }
 };
 
@@ -606,7 +635,7 @@ __device__ __forceinline__ uint32_t tile_count(const uint32_t *sbuf, const uint3
 // -- Day 33" (scatterPartition), with T the total kept from the pre-pass.
 // Both runs are compacted in place in the stage buffer(s) and written with
 // 128-bit stores.
-template <int THREADS, int ROWS, class Pred, bool VEC, bool VALS>
+template <int THREADS, int ROWS, class Pred, bool VEC, bool VALS, bool PLACED = false>
 struct PartitionOp {
     using TT = Tile<THREADS, ROWS>;
     static constexpr uint32_t kTileElems = TT::kElems;
@@ -620,10 +649,19 @@ struct PartitionOp {
     const uint32_t *true_total;  // written by the pre-pass kernel
     uint8_t *ws;
     Pred pred;
+    // Placed output (a shard of a larger partition): kept elements go to
+    // out[offsets[0] + rank], rejected ones to out[offsets[1] + i - rank],
+    // runs checked against capacity, and the last tile writes the tile
+    // total to count_out.  offsets == nullptr: the plain partition, kept
+    // from 0 and rejected from *true_total.
+    const uint64_t *offsets;
+    uint64_t capacity;
+    uint32_t *count_out;
 
     struct Carry {
         uint32_t mask[ROWS];
     };
+    __device__ __forceinline__ void seed(uint32_t &, float &, float &) const {}
     static constexpr bool kPreload = false;
     struct Loaded {};
 
@@ -662,23 +700,52 @@ struct PartitionOp {
                                   n, 0u, v[VALS ? r : 0]);
         }
         rank_masks<TT>(mask, lane_excl, s_chunk);
-        const uint32_t T = *true_total;
+        uint64_t kbase = 0u, rbase, cap = n;
+        if constexpr (PLACED) {
+            kbase = offsets[0];
+            rbase = offsets[1];
+            cap = capacity;
+        } else {
+            rbase = *true_total;
+        }
         __syncthreads();
         if (warp == 0) scan_chunks_warp0<TT>(s_chunk);
         __syncthreads();
 
         const uint32_t valid = min(kTileElems, n - base);
         uint32_t rejected = valid - kept;
-        const uint32_t dst_kept = before;
-        const uint32_t dst_rej = T + (base - before);
         uint32_t kept_len = kept;
-        // Both runs must lie inside [0, n), which holds when T is the true
-        // count; a wrong T (a workspace corrupted between the two kernels) is
-        // recorded and the stores are skipped.
-        if (uint64_t(dst_rej) + rejected > n || uint64_t(dst_kept) + kept > T) {
-            if (tid == 0) record_error(ws, kDeviceCheckCode, tile);
-            kept_len = 0u;
-            rejected = 0u;
+        if (PLACED && tid == 0 && last) *count_out = before + kept;
+        // Both runs must lie inside the output, which holds when T (or the
+        // placed offsets) are right; a wrong value (a workspace corrupted
+        // between the two kernels, a bad offset) is recorded and the stores
+        // are skipped.
+        uint32_t *kout_k = keys_out, *kout_r = keys_out, *vout_k = vals_out, *vout_r = vals_out;
+        uint32_t dst_kept, dst_rej;
+        if constexpr (PLACED) {
+            const uint64_t gk = kbase + before, gr = rbase + (base - before);
+            if (gr + rejected > cap || gk + kept > cap) {
+                if (tid == 0) record_error(ws, kDeviceCheckCode, tile);
+                kept_len = 0u;
+                rejected = 0u;
+            }
+            dst_kept = uint32_t(gk & 3u);
+            dst_rej = uint32_t(gr & 3u);
+            kout_k = keys_out + (gk & ~3ull);
+            kout_r = keys_out + (gr & ~3ull);
+            if (VALS) {
+                vout_k = vals_out + (gk & ~3ull);
+                vout_r = vals_out + (gr & ~3ull);
+            }
+        } else {
+            const uint32_t T = uint32_t(rbase);
+            dst_kept = before;
+            dst_rej = T + (base - before);
+            if (uint64_t(dst_rej) + rejected > cap || uint64_t(dst_kept) + kept > T) {
+                if (tid == 0) record_error(ws, kDeviceCheckCode, tile);
+                kept_len = 0u;
+                rejected = 0u;
+            }
         }
         const uint32_t sh_kept = VEC ? (dst_kept & 3u) : 0u;
         const uint32_t rej_region = (sh_kept + kept + 3u) & ~3u;
@@ -703,19 +770,19 @@ struct PartitionOp {
             // The runs leave by bulk copies from the stage buffer(s).
             fence_proxy_async_smem();
             __syncthreads();
-            store_run_bulk<THREADS>(keys_out, dst_kept, kbuf, sh_kept, kept_len, 0);
-            store_run_bulk<THREADS>(keys_out, dst_rej, kbuf, sh_rej, rejected, 1);
+            store_run_bulk<THREADS>(kout_k, dst_kept, kbuf, sh_kept, kept_len, 0);
+            store_run_bulk<THREADS>(kout_r, dst_rej, kbuf, sh_rej, rejected, 1);
             if (VALS) {
-                store_run_bulk<THREADS>(vals_out, dst_kept, vbuf, sh_kept, kept_len, 2);
-                store_run_bulk<THREADS>(vals_out, dst_rej, vbuf, sh_rej, rejected, 3);
+                store_run_bulk<THREADS>(vout_k, dst_kept, vbuf, sh_kept, kept_len, 2);
+                store_run_bulk<THREADS>(vout_r, dst_rej, vbuf, sh_rej, rejected, 3);
             }
         } else {
             __syncthreads();
-            store_run<THREADS, VEC>(keys_out, dst_kept, kbuf, sh_kept, kept_len);
-            store_run<THREADS, VEC>(keys_out, dst_rej, kbuf, sh_rej, rejected);
+            store_run<THREADS, VEC>(kout_k, dst_kept, kbuf, sh_kept, kept_len);
+            store_run<THREADS, VEC>(kout_r, dst_rej, kbuf, sh_rej, rejected);
             if (VALS) {
-                store_run<THREADS, VEC>(vals_out, dst_kept, vbuf, sh_kept, kept_len);
-                store_run<THREADS, VEC>(vals_out, dst_rej, vbuf, sh_rej, rejected);
+                store_run<THREADS, VEC>(vout_k, dst_kept, vbuf, sh_kept, kept_len);
+                store_run<THREADS, VEC>(vout_r, dst_rej, vbuf, sh_rej, rejected);
             }
         }
         (void)last;

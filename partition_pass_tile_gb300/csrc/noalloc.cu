@@ -22,11 +22,18 @@
 // status words, with an async memset first.  Calls whose work can overlap on
 // the GPU (different streams with no ordering between them) race on the
 // array and must not be issued.  The array starts zero-filled, as a
-// workspace must.
+// workspace must.  Failures inside a kernel are recorded in the array's
+// error word, which gc_select_if_noalloc_status reads and clears.
+//
+// The cached address belongs to the device's primary context: a
+// cudaDeviceReset destroys that context, and with it the array and every
+// cached value of this library, so the library must not be used across a
+// device reset.
 #include <cstring>
 #include <mutex>
 
 #include "../../include/gc.h"
+#include "../../include/gc_testing.h"
 #include "gc_internal.h"
 
 namespace {
@@ -64,11 +71,11 @@ bool overlaps(const void *a, size_t abytes, const void *b, size_t bbytes)
     return x < y + bbytes && y < x + abytes;
 }
 
-}  // namespace
-
-extern "C" gc_status gc_select_if_noalloc(const void *d_in, void *d_out, uint32_t *d_count,
-                                          size_t n, gc_dtype dtype, gc_pred pred,
-                                          cudaStream_t stream)
+// The entry point and its test hook: a hook may set the wait limit and mark
+// the start barrier before the call.
+gc_status select_if_noalloc(const void *d_in, void *d_out, uint32_t *d_count, size_t n,
+                            gc_dtype dtype, gc_pred pred, cudaStream_t stream,
+                            const gch::LaunchOpts &o, bool stall_barrier)
 {
     if (n > GC_NOALLOC_MAX_ELEMENTS) return GC_ERR_INVALID_VALUE;
     if (dtype != GC_I32 && dtype != GC_U32 && dtype != GC_F32) return GC_ERR_INVALID_VALUE;
@@ -93,8 +100,55 @@ extern "C" gc_status gc_select_if_noalloc(const void *d_in, void *d_out, uint32_
     if (n == 0)
         return cudaMemsetAsync(d_count, 0, sizeof(uint32_t), stream) == cudaSuccess ? GC_OK
                                                                                   : GC_ERR_CUDA;
-    const cudaError_t e = gch::launch_select(d_in, d_out, d_count, uint32_t(n), dtype, pred,
-                                             static_cast<uint8_t *>(scratch), stream,
-                                             gch::LaunchOpts{});
+    uint8_t *ws = static_cast<uint8_t *>(scratch);
+    if (stall_barrier &&
+        cudaMemsetAsync(ws + gch::kHdrBarArrive + 3, 0x80, 1, stream) != cudaSuccess)
+        return GC_ERR_CUDA;
+    const cudaError_t e = gch::launch_select(d_in, d_out, d_count, uint32_t(n), dtype, pred, ws,
+                                             stream, o);
     return e == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" gc_status gc_select_if_noalloc(const void *d_in, void *d_out, uint32_t *d_count,
+                                          size_t n, gc_dtype dtype, gc_pred pred,
+                                          cudaStream_t stream)
+{
+    return select_if_noalloc(d_in, d_out, d_count, n, dtype, pred, stream, gch::LaunchOpts{},
+                             false);
+}
+
+// Reads and clears the device-side error word of the array, as
+// gc_query_device_status does for a workspace; after an error also resets
+// the start barrier's arrival counter, which a barrier wait that gave up
+// leaves marked.  Synchronous: waits for the stream first.
+extern "C" gc_status gc_select_if_noalloc_status(cudaStream_t stream)
+{
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return GC_ERR_CUDA;
+    void *scratch = scratch_for_current_device();
+    if (scratch == nullptr) return GC_ERR_CUDA;
+    uint8_t *ws = static_cast<uint8_t *>(scratch);
+    uint32_t err = 0;
+    if (cudaMemcpy(&err, ws, sizeof err, cudaMemcpyDeviceToHost) != cudaSuccess) return GC_ERR_CUDA;
+    if (err == 0) return GC_OK;
+    const uint32_t zero[2] = {0, 0};
+    if (cudaMemcpy(ws, zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(ws + gch::kHdrBarArrive, zero, sizeof(uint32_t), cudaMemcpyHostToDevice) !=
+            cudaSuccess)
+        return GC_ERR_CUDA;
+    return (err == GC_ERR_TIMEOUT || err == GC_ERR_DEVICE_CHECK) ? gc_status(err) : GC_ERR_CUDA;
+}
+
+extern "C" gc_status gc_testing_select_if_noalloc_stalled_barrier(const void *d_in, void *d_out,
+                                                                   uint32_t *d_count, size_t n,
+                                                                   gc_dtype dtype, gc_pred pred,
+                                                                   uint64_t timeout_ns,
+                                                                   cudaStream_t stream)
+{
+    // the persistent kernel's path: the one with the start barrier
+    if (n == 0 || (reinterpret_cast<uintptr_t>(d_in) & 15u) != 0) return GC_ERR_INVALID_VALUE;
+    gch::LaunchOpts o;
+    o.timeout_ns = timeout_ns;
+    return select_if_noalloc(d_in, d_out, d_count, n, dtype, pred, stream, o, true);
 }

@@ -31,7 +31,8 @@ __global__ void __launch_bounds__(THREADS)
 partition_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__restrict__ vals_in,
                  uint32_t *__restrict__ keys_out, uint32_t *__restrict__ vals_out, uint32_t n,
                  uint32_t num_tiles, const uint32_t *true_total, Pred pred, uint8_t *ws,
-                 uint64_t timeout_ns)
+                 uint64_t timeout_ns, const uint64_t *offsets, uint64_t capacity,
+                 uint32_t *count_out)
 {
     using TT = Tile<THREADS, ROWS>;
     __shared__ uint32_t s_tile;
@@ -64,20 +65,29 @@ partition_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__restric
     rank_masks<TT>(mask, lane_excl, s_chunk);
     __syncthreads();
 
-    if (tid == 0) s_total = *true_total;
+    if (tid == 0 && offsets == nullptr) s_total = *true_total;
     uint32_t before, kept;
     resolve_prefix_u32<TT, LB>(s_chunk, tile, ws, timeout_ns, s_ps, before, kept);
+    if (tid == 0 && count_out != nullptr && tile == num_tiles - 1) *count_out = before + kept;
     const uint32_t valid = min(uint32_t(TT::kElems), n - base);
     const uint32_t rejected = valid - kept;
-    const uint32_t dst_kept = before;                      // rank of the tile's first kept element
-    const uint32_t dst_rej = s_total + (base - before);    // T + (i - rank[i]) at the tile start
-    // Both runs must lie inside [0, n): true only if T is the real count of
-    // kept elements.  A wrong T (a workspace corrupted between the kernels)
-    // is recorded and the stores are skipped instead of landing out of range.
-    if (uint64_t(dst_rej) + rejected > n || uint64_t(dst_kept) + kept > s_total) {
+    // Kept elements from kbase + rank[i], rejected ones from rbase + i - rank[i]
+    // (rbase = T for the plain partition, the placed offsets otherwise).
+    const uint64_t kbase = offsets != nullptr ? offsets[0] : 0u;
+    const uint64_t rbase = offsets != nullptr ? offsets[1] : s_total;
+    const uint64_t cap = offsets != nullptr ? capacity : n;
+    const uint64_t gk = kbase + before, gr = rbase + (base - before);
+    // Both runs must lie inside the output: true only if T (or the offsets)
+    // are right.  A wrong value (a workspace corrupted between the kernels) is
+    // recorded and the stores are skipped instead of landing out of range.
+    if (gr + rejected > cap || gk + kept > cap || (offsets == nullptr && gk + kept > rbase)) {
         if (tid == 0) record_error(ws, kDeviceCheckCode, tile);
         return;
     }
+    const uint32_t dst_kept = uint32_t(gk & 3u), dst_rej = uint32_t(gr & 3u);
+    uint32_t *const kout_k = keys_out + (gk & ~3ull), *const kout_r = keys_out + (gr & ~3ull);
+    uint32_t *const vout_k = VALS ? vals_out + (gk & ~3ull) : nullptr;
+    uint32_t *const vout_r = VALS ? vals_out + (gr & ~3ull) : nullptr;
     const uint32_t sh_kept = VEC ? (dst_kept & 3u) : 0u;
     const uint32_t rej_region = (sh_kept + kept + 3u) & ~3u;
     const uint32_t sh_rej = rej_region + (VEC ? (dst_rej & 3u) : 0u);
@@ -99,11 +109,11 @@ partition_kernel(const uint32_t *__restrict__ keys_in, const uint32_t *__restric
         }
     }
     __syncthreads();
-    store_run<THREADS, VEC>(keys_out, dst_kept, s_keys, sh_kept, kept);
-    store_run<THREADS, VEC>(keys_out, dst_rej, s_keys, sh_rej, rejected);
+    store_run<THREADS, VEC>(kout_k, dst_kept, s_keys, sh_kept, kept);
+    store_run<THREADS, VEC>(kout_r, dst_rej, s_keys, sh_rej, rejected);
     if (VALS) {
-        store_run<THREADS, VEC>(vals_out, dst_kept, s_vals, sh_kept, kept);
-        store_run<THREADS, VEC>(vals_out, dst_rej, s_vals, sh_rej, rejected);
+        store_run<THREADS, VEC>(vout_k, dst_kept, s_vals, sh_kept, kept);
+        store_run<THREADS, VEC>(vout_r, dst_rej, s_vals, sh_rej, rejected);
     }
 }
 
@@ -295,10 +305,19 @@ int reduce_grid(uint32_t n, int threads)
     return int(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
+// Where a partition pass puts its runs: the plain partition (offsets null:
+// kept from 0, rejected from the device-side T) or a placed shard.
+struct PartPlace {
+    const uint64_t *offsets = nullptr;
+    uint64_t capacity = 0;
+    uint32_t *count_out = nullptr;
+};
+
 template <int PT, int PR, int PS, class Pred, bool VALS>
 cudaError_t run_partition_pipe(const uint32_t *kin, const uint32_t *vin, uint32_t *kout,
                                uint32_t *vout, uint32_t n, const uint32_t *true_total, Pred pred,
-                               uint8_t *ws, cudaStream_t s, const gch::LaunchOpts &o)
+                               uint8_t *ws, cudaStream_t s, const gch::LaunchOpts &o,
+                               const PartPlace &pl)
 {
     const bool vec = gch::aligned16(kout) && (!VALS || gch::aligned16(vout));
     auto fill = [&](auto &op) {
@@ -309,15 +328,26 @@ cudaError_t run_partition_pipe(const uint32_t *kin, const uint32_t *vin, uint32_
         op.true_total = true_total;
         op.ws = ws;
         op.pred = pred;
+        op.offsets = pl.offsets;
+        op.capacity = pl.capacity;
+        op.count_out = pl.count_out;
     };
-    if (vec) {
-        gcd::PartitionOp<PT, PR, Pred, true, VALS> op{};
+    auto go = [&](auto op) {
         fill(op);
         return gcd::launch_pipeline<PT, PS>(op, n, ws, s, o);
+    };
+    // The placed form (a shard of a larger partition) is its own
+    // instantiation, so the plain partition and the radix splits keep their
+    // 32-bit addressing.
+    if (pl.offsets != nullptr) {
+        if constexpr (!VALS) {
+            if (vec) return go(gcd::PartitionOp<PT, PR, Pred, true, VALS, true>{});
+            return go(gcd::PartitionOp<PT, PR, Pred, false, VALS, true>{});
+        }
+        return cudaErrorNotSupported;
     }
-    gcd::PartitionOp<PT, PR, Pred, false, VALS> op{};
-    fill(op);
-    return gcd::launch_pipeline<PT, PS>(op, n, ws, s, o);
+    if (vec) return go(gcd::PartitionOp<PT, PR, Pred, true, VALS, false>{});
+    return go(gcd::PartitionOp<PT, PR, Pred, false, VALS, false>{});
 }
 
 // *piped (optional) says whether the persistent kernel ran; the fallback
@@ -327,17 +357,17 @@ template <class Pred, bool VALS>
 cudaError_t run_partition_pass(const uint32_t *kin, const uint32_t *vin, uint32_t *kout,
                                uint32_t *vout, uint32_t n, const uint32_t *true_total, Pred pred,
                                uint8_t *ws, cudaStream_t s, const gch::LaunchOpts &o, bool split,
-                               bool *piped = nullptr)
+                               bool *piped = nullptr, const PartPlace &pl = PartPlace{})
 {
     if (piped != nullptr) *piped = false;
     if (gch::aligned16(kin) && (!VALS || gch::aligned16(vin)) && !o.skip_first_tile) {
         cudaError_t e;
         if (split)
             e = run_partition_pipe<gch::kSplitPipeThreads, gch::kSplitPipeRows, gch::kSplitPipeStages,
-                                   Pred, VALS>(kin, vin, kout, vout, n, true_total, pred, ws, s, o);
+                                   Pred, VALS>(kin, vin, kout, vout, n, true_total, pred, ws, s, o, pl);
         else
             e = run_partition_pipe<gch::kPartPipeThreads, gch::kPartPipeRows, gch::kPartPipeStages,
-                                   Pred, VALS>(kin, vin, kout, vout, n, true_total, pred, ws, s, o);
+                                   Pred, VALS>(kin, vin, kout, vout, n, true_total, pred, ws, s, o, pl);
         if (e == cudaSuccess) {
             if (piped != nullptr) *piped = true;
             return e;
@@ -357,17 +387,17 @@ cudaError_t run_partition_pass(const uint32_t *kin, const uint32_t *vin, uint32_
     if (split) {
         if (vec)
             partition_kernel<Pred, ST, SR, true, VALS, gch::kCtaLookback><<<grid, ST, 0, s>>>(
-                kin, vin, kout, vout, n, tiles, true_total, pred, ws, o.timeout_ns);
+                kin, vin, kout, vout, n, tiles, true_total, pred, ws, o.timeout_ns, pl.offsets, pl.capacity, pl.count_out);
         else
             partition_kernel<Pred, ST, SR, false, VALS, gch::kCtaLookback><<<grid, ST, 0, s>>>(
-                kin, vin, kout, vout, n, tiles, true_total, pred, ws, o.timeout_ns);
+                kin, vin, kout, vout, n, tiles, true_total, pred, ws, o.timeout_ns, pl.offsets, pl.capacity, pl.count_out);
     } else {
         if (vec)
             partition_kernel<Pred, PT, PR, true, VALS, gch::kCtaLookback><<<grid, PT, 0, s>>>(
-                kin, vin, kout, vout, n, tiles, true_total, pred, ws, o.timeout_ns);
+                kin, vin, kout, vout, n, tiles, true_total, pred, ws, o.timeout_ns, pl.offsets, pl.capacity, pl.count_out);
         else
             partition_kernel<Pred, PT, PR, false, VALS, gch::kCtaLookback><<<grid, PT, 0, s>>>(
-                kin, vin, kout, vout, n, tiles, true_total, pred, ws, o.timeout_ns);
+                kin, vin, kout, vout, n, tiles, true_total, pred, ws, o.timeout_ns, pl.offsets, pl.capacity, pl.count_out);
     }
     return cudaGetLastError();
 }
@@ -391,6 +421,37 @@ cudaError_t dispatch_partition(const uint32_t *in, uint32_t *out, uint32_t *coun
     return run_partition_pass<Pred, false>(in, nullptr, out, nullptr, n, T, pred, ws, s, o, false);
 }
 
+// A shard of a larger partition: the offsets are known (from the counts of
+// every shard), so no pre-pass; one pass writes both runs and the count.
+template <class Pred>
+cudaError_t dispatch_partition_at(const uint32_t *in, uint32_t *out, uint64_t capacity,
+                                  const uint64_t *offsets, uint32_t *count_true, uint32_t n,
+                                  Pred pred, uint8_t *ws, cudaStream_t s, const gch::LaunchOpts &o)
+{
+    PartPlace pl;
+    pl.offsets = offsets;
+    pl.capacity = capacity;
+    pl.count_out = count_true;
+    return run_partition_pass<Pred, false>(in, nullptr, out, nullptr, n, nullptr, pred, ws, s, o,
+                                           false, nullptr, pl);
+}
+
+// Count pre-pass alone (gc_count_if).
+template <class Pred>
+cudaError_t dispatch_count(const uint32_t *in, uint32_t *count, uint32_t n, Pred pred, uint8_t *ws,
+                           cudaStream_t s)
+{
+    constexpr int RT = gch::kReduceThreads;
+    const int grid = reduce_grid(n, RT);
+    cudaError_t e0 = gch::clear_accumulators(ws, s);
+    if (e0 != cudaSuccess) return e0;
+    if (gch::aligned16(in))
+        count_kernel<Pred, RT, true><<<grid, RT, 0, s>>>(in, n, pred, ws, count);
+    else
+        count_kernel<Pred, RT, false><<<grid, RT, 0, s>>>(in, n, pred, ws, count);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 namespace gch {
@@ -410,6 +471,36 @@ cudaError_t launch_partition(const void *in, void *out, uint32_t *count_true, ui
         return dispatch_partition(i, u, count_true, n, gcd::PredNonzeroInt{}, ws, s, o);
     case GC_PRED_ODD: return dispatch_partition(i, u, count_true, n, gcd::PredOdd{}, ws, s, o);
     default: return dispatch_partition(i, u, count_true, n, gcd::PredEven{}, ws, s, o);
+    }
+}
+
+cudaError_t launch_partition_at(const void *in, void *out, uint64_t capacity,
+                                const uint64_t *offsets, uint32_t *count_true, uint32_t n,
+                                gc_dtype dt, gc_pred p, uint8_t *ws, cudaStream_t s,
+                                const LaunchOpts &o)
+{
+    auto *i = static_cast<const uint32_t *>(in);
+    auto *u = static_cast<uint32_t *>(out);
+    switch (p) {
+    case GC_PRED_NONZERO:
+        if (dt == GC_F32)
+            return dispatch_partition_at(i, u, capacity, offsets, count_true, n, gcd::PredNonzeroF32{}, ws, s, o);
+        return dispatch_partition_at(i, u, capacity, offsets, count_true, n, gcd::PredNonzeroInt{}, ws, s, o);
+    case GC_PRED_ODD: return dispatch_partition_at(i, u, capacity, offsets, count_true, n, gcd::PredOdd{}, ws, s, o);
+    default: return dispatch_partition_at(i, u, capacity, offsets, count_true, n, gcd::PredEven{}, ws, s, o);
+    }
+}
+
+cudaError_t launch_count_if(const void *in, uint32_t *count, uint32_t n, gc_dtype dt, gc_pred p,
+                            uint8_t *ws, cudaStream_t s)
+{
+    auto *i = static_cast<const uint32_t *>(in);
+    switch (p) {
+    case GC_PRED_NONZERO:
+        if (dt == GC_F32) return dispatch_count(i, count, n, gcd::PredNonzeroF32{}, ws, s);
+        return dispatch_count(i, count, n, gcd::PredNonzeroInt{}, ws, s);
+    case GC_PRED_ODD: return dispatch_count(i, count, n, gcd::PredOdd{}, ws, s);
+    default: return dispatch_count(i, count, n, gcd::PredEven{}, ws, s);
     }
 }
 

@@ -20,6 +20,8 @@
 // In place (in == out) is safe: each element is read before the barriers
 // and written after them by the same thread, and no thread touches another
 // thread's elements.
+#include <algorithm>
+
 #include "gc_device.cuh"
 #include "gc_internal.h"
 #include "gc_launch.cuh"
@@ -31,7 +33,7 @@ using namespace gcd;
 template <int THREADS, int ROWS, bool VEC, bool LB, bool INCL>
 __global__ void __launch_bounds__(THREADS)
 scan_u32_kernel(const uint32_t *in, uint32_t *out, uint32_t *total, uint32_t n,
-                uint32_t num_tiles, uint8_t *ws, uint64_t timeout_ns)
+                uint32_t num_tiles, uint8_t *ws, uint64_t timeout_ns, const uint32_t *carry)
 {
     using TT = Tile<THREADS, ROWS>;
     __shared__ uint32_t s_tile;
@@ -65,6 +67,7 @@ scan_u32_kernel(const uint32_t *in, uint32_t *out, uint32_t *total, uint32_t n,
 
     uint32_t prefix, agg;
     resolve_prefix_u32<TT, LB>(s_chunk, tile, ws, timeout_ns, s_ps, prefix, agg);
+    if (carry != nullptr) prefix += *carry;  // the look-back itself stays carry-free
     if (tid == 0 && total != nullptr && tile == num_tiles - 1) *total = prefix + agg;
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
@@ -88,7 +91,8 @@ scan_u32_kernel(const uint32_t *in, uint32_t *out, uint32_t *total, uint32_t n,
 template <int THREADS, int ROWS, bool VEC, bool LB, bool INCL>
 __global__ void __launch_bounds__(THREADS)
 scan_f32_kernel(const uint32_t *in_bits, uint32_t *out_bits, uint32_t *total_bits, uint32_t n,
-                uint32_t num_tiles, uint8_t *ws, double *prefix64, uint64_t timeout_ns)
+                uint32_t num_tiles, uint8_t *ws, double *prefix64, uint64_t timeout_ns,
+                const uint32_t *carry)
 {
     using TT = Tile<THREADS, ROWS>;
     __shared__ uint32_t s_tile;
@@ -125,6 +129,7 @@ scan_f32_kernel(const uint32_t *in_bits, uint32_t *out_bits, uint32_t *total_bit
     double excl;
     float agg;
     resolve_prefix_f32<TT, LB>(s_chunk, tile, ws, prefix64, timeout_ns, s_ps, excl, agg);
+    if (carry != nullptr) excl += double(__uint_as_float(*carry));
     if (tid == 0 && total_bits != nullptr && tile == num_tiles - 1)
         *total_bits = __float_as_uint(float(excl + double(agg)));
     const float hi = float(excl);
@@ -143,9 +148,114 @@ scan_f32_kernel(const uint32_t *in_bits, uint32_t *out_bits, uint32_t *total_bit
     }
 }
 
+// Sum of the n elements, the aggregate half of the scan alone: the pre-pass
+// of a scan split over shards, whose offsets need every shard's total before
+// any shard is scanned.  Grid-stride 128-bit loads; int32 / uint32 add modulo
+// 2^32, float32 sums each 4-vector in float and accumulates the vector sums
+// per thread as a float pair (TwoSum), so the thread's error stays near one
+// rounding of its total.  Each CTA stores its partial in the workspace's
+// status area; the CTA that finishes last (ticket counter) adds the partials
+// in CTA order (float32 in double) and writes the total, so the result does
+// not depend on the order in which CTAs finish.
+template <bool F32, bool VEC>
+__global__ void __launch_bounds__(256)
+reduce_kernel(const uint32_t *__restrict__ in, uint32_t n, uint8_t *ws, uint32_t *total)
+{
+    constexpr int W = 256 / 32;
+    __shared__ float s_h[W], s_l[W];
+    __shared__ uint32_t s_u[W];
+    __shared__ uint32_t s_last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t nvec = (n + 3u) / 4u;
+    const uint32_t stride = gridDim.x * 256u;
+    uint32_t su = 0u;
+    float h = 0.0f, l = 0.0f;
+    for (uint32_t v = blockIdx.x * 256u + tid; v < nvec; v += stride) {
+        uint32_t x[4];
+        load4<VEC>(in, 4u * v, n, 0u, x);
+        if (F32) {
+            const float a = (__uint_as_float(x[0]) + __uint_as_float(x[1])) +
+                            (__uint_as_float(x[2]) + __uint_as_float(x[3]));
+            ff_add(h, l, a, 0.0f, h, l);
+        } else {
+            su += x[0] + x[1] + x[2] + x[3];
+        }
+    }
+    uint64_t *partial = reinterpret_cast<uint64_t *>(ws + kStatusOff);
+    if (F32) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float oh = __shfl_xor_sync(kFullMask, h, o), ol = __shfl_xor_sync(kFullMask, l, o);
+            ff_add(h, l, oh, ol, h, l);
+        }
+        if (lane == 0) {
+            s_h[warp] = h;
+            s_l[warp] = l;
+        }
+    } else {
+        su = warp_sum(su);
+        if (lane == 0) s_u[warp] = su;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        uint64_t word;
+        if (F32) {
+            float th = 0.0f, tl = 0.0f;
+            for (int w = 0; w < W; ++w) ff_add(th, tl, s_h[w], s_l[w], th, tl);
+            word = (uint64_t(__float_as_uint(tl)) << 32) | __float_as_uint(th);
+        } else {
+            uint32_t t = 0u;
+            for (int w = 0; w < W; ++w) t += s_u[w];
+            word = t;
+        }
+        st_relaxed_gpu(partial + blockIdx.x, word);
+        __threadfence();
+        s_last = atomicAdd(hdr_u32(ws, kHdrReduceCtr), 1u) == gridDim.x - 1u ? 1u : 0u;
+    }
+    __syncthreads();
+    if (s_last == 0u || tid != 0) return;
+    __threadfence();
+    if (F32) {
+        double acc = 0.0;
+        for (uint32_t b = 0; b < gridDim.x; ++b) {
+            const uint64_t w = ld_relaxed_gpu(partial + b);
+            acc += double(__uint_as_float(uint32_t(w))) + double(__uint_as_float(uint32_t(w >> 32)));
+        }
+        *total = __float_as_uint(float(acc));
+    } else {
+        uint32_t acc = 0u;
+        for (uint32_t b = 0; b < gridDim.x; ++b) acc += uint32_t(ld_relaxed_gpu(partial + b));
+        *total = acc;
+    }
+    atomicExch(hdr_u32(ws, kHdrReduceCtr), 0u);
+}
+
 }  // namespace
 
 namespace gch {
+
+cudaError_t launch_reduce(const void *in, void *total, uint32_t n, gc_dtype dt, uint8_t *ws,
+                          cudaStream_t s)
+{
+    auto *i = static_cast<const uint32_t *>(in);
+    auto *t = static_cast<uint32_t *>(total);
+    // Partials take one status word per CTA: never more CTAs than the
+    // workspace has words for.
+    const size_t want = ceil_div(ceil_div(n, 4), 256);
+    size_t grid = std::min<size_t>(want, size_t(sm_count()) * 8);
+    grid = std::max<size_t>(1, std::min(grid, max_tiles(n)));
+    cudaError_t e = clear_accumulators(ws, s);
+    if (e != cudaSuccess) return e;
+    const bool vec = aligned16(in);
+    if (dt == GC_F32) {
+        if (vec) reduce_kernel<true, true><<<unsigned(grid), 256, 0, s>>>(i, n, ws, t);
+        else reduce_kernel<true, false><<<unsigned(grid), 256, 0, s>>>(i, n, ws, t);
+    } else {
+        if (vec) reduce_kernel<false, true><<<unsigned(grid), 256, 0, s>>>(i, n, ws, t);
+        else reduce_kernel<false, false><<<unsigned(grid), 256, 0, s>>>(i, n, ws, t);
+    }
+    return cudaGetLastError();
+}
 
 uint32_t scan_tile_elems() { return tile_elems(kScanPipeThreads, kScanPipeRows); }
 
@@ -153,29 +263,31 @@ namespace {
 
 template <bool F32, bool OUT_VEC, bool INCL>
 cudaError_t launch_scan_pipe(const uint32_t *in, uint32_t *out, uint32_t *total, uint32_t n,
-                             uint8_t *ws, cudaStream_t s, const LaunchOpts &o)
+                             uint8_t *ws, cudaStream_t s, const LaunchOpts &o,
+                             const uint32_t *carry)
 {
     using Op = gcd::ScanOp<kScanPipeThreads, kScanPipeRows, F32, OUT_VEC, INCL>;
-    Op op{{in}, out, total};
+    Op op{{in}, out, total, carry};
     return gcd::launch_pipeline<kScanPipeThreads, kScanPipeStages>(op, n, ws, s, o);
 }
 
 template <bool INCL>
 cudaError_t launch_scan_impl(const void *in, void *out, void *total, uint32_t n, gc_dtype dt,
-                             uint8_t *ws, cudaStream_t s, const LaunchOpts &o)
+                             uint8_t *ws, cudaStream_t s, const LaunchOpts &o, const void *carry)
 {
     auto *i = static_cast<const uint32_t *>(in);
     auto *u = static_cast<uint32_t *>(out);
     auto *t = static_cast<uint32_t *>(total);
+    auto *c = static_cast<const uint32_t *>(carry);
     cudaError_t e;
     if (aligned16(in) && !o.skip_first_tile) {
         const bool ov = aligned16(out);
         if (dt == GC_F32)
-            e = ov ? launch_scan_pipe<true, true, INCL>(i, u, t, n, ws, s, o)
-                   : launch_scan_pipe<true, false, INCL>(i, u, t, n, ws, s, o);
+            e = ov ? launch_scan_pipe<true, true, INCL>(i, u, t, n, ws, s, o, c)
+                   : launch_scan_pipe<true, false, INCL>(i, u, t, n, ws, s, o, c);
         else
-            e = ov ? launch_scan_pipe<false, true, INCL>(i, u, t, n, ws, s, o)
-                   : launch_scan_pipe<false, false, INCL>(i, u, t, n, ws, s, o);
+            e = ov ? launch_scan_pipe<false, true, INCL>(i, u, t, n, ws, s, o, c)
+                   : launch_scan_pipe<false, false, INCL>(i, u, t, n, ws, s, o, c);
         if (e == cudaSuccess) return e;
         // The device cannot hold the whole cooperative grid right now (another
         // context holds SMs): fall through to the kernel that needs no
@@ -195,17 +307,17 @@ cudaError_t launch_scan_impl(const void *in, void *out, void *total, uint32_t n,
         double *prefix64 = reinterpret_cast<double *>(ws + kHeaderBytes + status_bytes(tiles));
         if (vec)
             scan_f32_kernel<kScanThreads, kScanRows, true, kCtaLookback, INCL>
-                <<<grid, kScanThreads, 0, s>>>(i, u, t, n, tiles, ws, prefix64, o.timeout_ns);
+                <<<grid, kScanThreads, 0, s>>>(i, u, t, n, tiles, ws, prefix64, o.timeout_ns, c);
         else
             scan_f32_kernel<kScanThreads, kScanRows, false, kCtaLookback, INCL>
-                <<<grid, kScanThreads, 0, s>>>(i, u, t, n, tiles, ws, prefix64, o.timeout_ns);
+                <<<grid, kScanThreads, 0, s>>>(i, u, t, n, tiles, ws, prefix64, o.timeout_ns, c);
     } else {
         if (vec)
             scan_u32_kernel<kScanThreads, kScanRows, true, kCtaLookback, INCL>
-                <<<grid, kScanThreads, 0, s>>>(i, u, t, n, tiles, ws, o.timeout_ns);
+                <<<grid, kScanThreads, 0, s>>>(i, u, t, n, tiles, ws, o.timeout_ns, c);
         else
             scan_u32_kernel<kScanThreads, kScanRows, false, kCtaLookback, INCL>
-                <<<grid, kScanThreads, 0, s>>>(i, u, t, n, tiles, ws, o.timeout_ns);
+                <<<grid, kScanThreads, 0, s>>>(i, u, t, n, tiles, ws, o.timeout_ns, c);
     }
     return cudaGetLastError();
 }
@@ -213,10 +325,11 @@ cudaError_t launch_scan_impl(const void *in, void *out, void *total, uint32_t n,
 }  // namespace
 
 cudaError_t launch_scan(const void *in, void *out, void *total, uint32_t n, gc_dtype dt,
-                        uint8_t *ws, cudaStream_t s, const LaunchOpts &o, bool inclusive)
+                        uint8_t *ws, cudaStream_t s, const LaunchOpts &o, bool inclusive,
+                        const void *carry)
 {
-    return inclusive ? launch_scan_impl<true>(in, out, total, n, dt, ws, s, o)
-                     : launch_scan_impl<false>(in, out, total, n, dt, ws, s, o);
+    return inclusive ? launch_scan_impl<true>(in, out, total, n, dt, ws, s, o, carry)
+                     : launch_scan_impl<false>(in, out, total, n, dt, ws, s, o, carry);
 }
 
 }  // namespace gch

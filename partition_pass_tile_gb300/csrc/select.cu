@@ -34,7 +34,8 @@ using namespace gcd;
 template <class Pred, int THREADS, int ROWS, bool VEC, bool LB>
 __global__ void __launch_bounds__(THREADS)
 select_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, uint32_t *count,
-              uint32_t n, uint32_t num_tiles, Pred pred, uint8_t *ws, uint64_t timeout_ns)
+              uint32_t n, uint32_t num_tiles, Pred pred, uint8_t *ws, uint64_t timeout_ns,
+              SelectPlacement place)
 {
     using TT = Tile<THREADS, ROWS>;
     __shared__ uint32_t s_tile;
@@ -63,9 +64,17 @@ select_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, uint3
     rank_masks<TT>(mask, lane_excl, s_chunk);
     __syncthreads();
 
-    uint32_t out_base, kept;
-    resolve_prefix_u32<TT, LB>(s_chunk, tile, ws, timeout_ns, s_ps, out_base, kept);
-    if (tid == 0 && tile == num_tiles - 1) *count = out_base + kept;
+    uint32_t prefix, kept;
+    resolve_prefix_u32<TT, LB>(s_chunk, tile, ws, timeout_ns, s_ps, prefix, kept);
+    if (tid == 0 && tile == num_tiles - 1) *count = prefix + kept;
+    // survivors go to out[obase + prefix + rank] (obase = 0 unless placed)
+    const uint64_t ob = place.obase != nullptr ? *place.obase : 0ull;
+    if (ob + uint64_t(prefix) + kept > place.cap) {
+        if (tid == 0) record_error(ws, kDeviceCheckCode, tile);
+        return;
+    }
+    out += ob & ~3ull;
+    const uint32_t out_base = uint32_t(ob & 3ull) + prefix;
     const uint32_t shift = VEC ? (out_base & 3u) : 0u;
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
@@ -166,17 +175,18 @@ select_atomic_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out
 
 template <class Pred>
 cudaError_t dispatch_select(const uint32_t *in, uint32_t *out, uint32_t *count, uint32_t n,
-                            Pred pred, uint8_t *ws, cudaStream_t s, const gch::LaunchOpts &o)
+                            Pred pred, uint8_t *ws, cudaStream_t s, const gch::LaunchOpts &o,
+                            SelectPlacement place)
 {
     if (gch::aligned16(in) && !o.skip_first_tile) {
         constexpr int PT = gch::kSelectPipeThreads, PR = gch::kSelectPipeRows;
         constexpr int PS = gch::kSelectPipeStages;
         cudaError_t e;
         if (gch::aligned16(out)) {
-            gcd::SelectOp<PT, PR, Pred, true> op{{in}, out, count, pred};
+            gcd::SelectOp<PT, PR, Pred, true> op{{in}, out, count, pred, place, ws};
             e = gcd::launch_pipeline<PT, PS>(op, n, ws, s, o);
         } else {
-            gcd::SelectOp<PT, PR, Pred, false> op{{in}, out, count, pred};
+            gcd::SelectOp<PT, PR, Pred, false> op{{in}, out, count, pred, place, ws};
             e = gcd::launch_pipeline<PT, PS>(op, n, ws, s, o);
         }
         if (e == cudaSuccess) return e;
@@ -189,9 +199,9 @@ cudaError_t dispatch_select(const uint32_t *in, uint32_t *out, uint32_t *count, 
     const uint32_t grid = o.skip_first_tile ? tiles - 1 : tiles;
     if (grid == 0) return cudaSuccess;
     if (gch::aligned16(in) && gch::aligned16(out))
-        select_kernel<Pred, T, R, true, gch::kCtaLookback><<<grid, T, 0, s>>>(in, out, count, n, tiles, pred, ws, o.timeout_ns);
+        select_kernel<Pred, T, R, true, gch::kCtaLookback><<<grid, T, 0, s>>>(in, out, count, n, tiles, pred, ws, o.timeout_ns, place);
     else
-        select_kernel<Pred, T, R, false, gch::kCtaLookback><<<grid, T, 0, s>>>(in, out, count, n, tiles, pred, ws, o.timeout_ns);
+        select_kernel<Pred, T, R, false, gch::kCtaLookback><<<grid, T, 0, s>>>(in, out, count, n, tiles, pred, ws, o.timeout_ns, place);
     return cudaGetLastError();
 }
 
@@ -244,16 +254,18 @@ uint32_t select_tile_elems() { return tile_elems(kSelectPipeThreads, kSelectPipe
 uint32_t atomic_tile_elems() { return tile_elems(kAtomicThreads, kAtomicRows); }
 
 cudaError_t launch_select(const void *in, void *out, uint32_t *count, uint32_t n, gc_dtype dt,
-                          gc_pred p, uint8_t *ws, cudaStream_t s, const LaunchOpts &o)
+                          gc_pred p, uint8_t *ws, cudaStream_t s, const LaunchOpts &o,
+                          const uint64_t *obase, uint64_t cap)
 {
     auto *i = static_cast<const uint32_t *>(in);
     auto *u = static_cast<uint32_t *>(out);
+    const gcd::SelectPlacement place{obase, obase != nullptr ? cap : uint64_t(n)};
     switch (p) {
     case GC_PRED_NONZERO:
-        if (dt == GC_F32) return dispatch_select(i, u, count, n, gcd::PredNonzeroF32{}, ws, s, o);
-        return dispatch_select(i, u, count, n, gcd::PredNonzeroInt{}, ws, s, o);
-    case GC_PRED_ODD: return dispatch_select(i, u, count, n, gcd::PredOdd{}, ws, s, o);
-    default: return dispatch_select(i, u, count, n, gcd::PredEven{}, ws, s, o);
+        if (dt == GC_F32) return dispatch_select(i, u, count, n, gcd::PredNonzeroF32{}, ws, s, o, place);
+        return dispatch_select(i, u, count, n, gcd::PredNonzeroInt{}, ws, s, o, place);
+    case GC_PRED_ODD: return dispatch_select(i, u, count, n, gcd::PredOdd{}, ws, s, o, place);
+    default: return dispatch_select(i, u, count, n, gcd::PredEven{}, ws, s, o, place);
     }
 }
 
@@ -262,11 +274,12 @@ cudaError_t launch_select_cmp(const void *in, void *out, uint32_t *count, uint32
 {
     auto *i = static_cast<const uint32_t *>(in);
     auto *u = static_cast<uint32_t *>(out);
+    const gcd::SelectPlacement place{nullptr, uint64_t(n)};
     if (dt == GC_I32)
-        return dispatch_select(i, u, count, n, gcd::PredCmp<0>{c.lo, c.span, c.invert, c.is_mask, c.mask, c.value}, ws, s, o);
+        return dispatch_select(i, u, count, n, gcd::PredCmp<0>{c.lo, c.span, c.invert, c.is_mask, c.mask, c.value}, ws, s, o, place);
     if (dt == GC_U32)
-        return dispatch_select(i, u, count, n, gcd::PredCmp<1>{c.lo, c.span, c.invert, c.is_mask, c.mask, c.value}, ws, s, o);
-    return dispatch_select(i, u, count, n, gcd::PredCmp<2>{c.lo, c.span, c.invert, c.is_mask, c.mask, c.value}, ws, s, o);
+        return dispatch_select(i, u, count, n, gcd::PredCmp<1>{c.lo, c.span, c.invert, c.is_mask, c.mask, c.value}, ws, s, o, place);
+    return dispatch_select(i, u, count, n, gcd::PredCmp<2>{c.lo, c.span, c.invert, c.is_mask, c.mask, c.value}, ws, s, o, place);
 }
 
 cudaError_t launch_select_atomic(const void *in, void *out, uint32_t *count, uint32_t n,

@@ -26,6 +26,8 @@ NONZERO, ODD, EVEN = 0, 1, 2
 OP_EXCLUSIVE_SCAN, OP_SELECT_IF, OP_PARTITION, OP_SPLIT_RADIX, OP_SELECT_IF_ATOMIC = range(5)
 OP_INCLUSIVE_SCAN = 5
 OP_RADIX_SORT = 6
+OP_REDUCE = 7
+OP_COUNT_IF = 8
 LT, LE, GT, GE, EQ, NE, MASK_EQ, MASK_NE = range(8)
 CMP_NAMES = {"<": LT, "<=": LE, ">": GT, ">=": GE, "==": EQ, "!=": NE,
              "mask==": MASK_EQ, "mask!=": MASK_NE}
@@ -79,6 +81,12 @@ def load(path: str | Path | None = None) -> ctypes.CDLL:
         "gc_select_if_pred": ([V, V, V, Z, I, ctypes.POINTER(Predicate), V, Z, V], S),
         "gc_partition_pred": ([V, V, V, Z, I, ctypes.POINTER(Predicate), V, Z, V], S),
         "gc_radix_sort": ([V, V, V, V, Z, I, V, Z, V], S),
+        "gc_reduce": ([V, V, Z, I, V, Z, V], S),
+        "gc_count_if": ([V, V, Z, I, I, V, Z, V], S),
+        "gc_shard_offsets": ([I, I, V, ctypes.POINTER(U64), Z, Z, V, V], S),
+        "gc_exclusive_scan_carry": ([V, V, V, Z, I, V, V, Z, V], S),
+        "gc_select_if_at": ([V, V, Z, V, V, Z, I, I, V, Z, V], S),
+        "gc_partition_at": ([V, V, Z, V, V, Z, I, I, V, Z, V], S),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -332,6 +340,26 @@ def testing_exclusive_scan_stalled_barrier(x: torch.Tensor, out, total, ws, time
 NOALLOC_MAX_ELEMENTS = 1 << 28
 
 
+def select_if_noalloc_status(stream=None) -> int:
+    """Synchronous: the no-workspace entry point's device-side error code
+    (0 = none) on the current device, then cleared."""
+    f = load().gc_select_if_noalloc_status
+    f.argtypes = [ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    return int(f(_stream(stream)))
+
+
+def testing_select_if_noalloc_stalled_barrier(x: torch.Tensor, pred, out, count, timeout_ns: int,
+                                              stream=None) -> int:
+    """Test hook (include/gc_testing.h): returns the launch status."""
+    f = load().gc_testing_select_if_noalloc_stalled_barrier
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    return int(f(_ptr(x), _ptr(out), _ptr(count), x.numel(), dtype_code(x), pred_code(pred),
+                 timeout_ns, _stream(stream)))
+
+
 def select_if_noalloc(x: torch.Tensor, pred, out: torch.Tensor | None = None,
                       count: torch.Tensor | None = None, stream=None):
     """gc_select_if_noalloc: select-if with the library's own fixed scratch
@@ -348,3 +376,102 @@ def select_if_noalloc(x: torch.Tensor, pred, out: torch.Tensor | None = None,
     _check(f(_ptr(x), _ptr(out), _ptr(count), x.numel(), dtype_code(x), pred_code(pred),
              _stream(stream)), "gc_select_if_noalloc")
     return out, count
+
+
+# ---------------------------------------------------------------- shards
+
+def reduce(x: torch.Tensor, total: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+           stream=None) -> torch.Tensor:
+    """gc_reduce: a 1-element device tensor of x's dtype holding sum(x)."""
+    n = x.numel()
+    dt = dtype_code(x)
+    if total is None:
+        total = torch.empty(1, dtype=x.dtype, device=x.device)
+    ws = _ws(ws, OP_REDUCE, n, dt, x.device)
+    _check(load().gc_reduce(_ptr(x), _ptr(total), n, dt, _ptr(ws), ws.numel(), _stream(stream)),
+           "gc_reduce")
+    return total
+
+
+def count_if(x: torch.Tensor, pred, count: torch.Tensor | None = None,
+             ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """gc_count_if: a 1-element uint32 device tensor, how many elements pred keeps."""
+    n = x.numel()
+    dt = dtype_code(x)
+    if count is None:
+        count = torch.empty(1, dtype=torch.uint32, device=x.device)
+    ws = _ws(ws, OP_COUNT_IF, n, dt, x.device)
+    _check(load().gc_count_if(_ptr(x), _ptr(count), n, dt, pred_code(pred), _ptr(ws), ws.numel(),
+                              _stream(stream)), "gc_count_if")
+    return count
+
+
+def shard_offsets(op: int, totals: torch.Tensor, rank: int, sizes=None, dtype: int | None = None,
+                  out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """gc_shard_offsets for shard `rank` of totals.numel() shards.  Returns one
+    element of totals' dtype (scan), one 64-bit offset (select-if) or two
+    (partition: kept before, first rejected position; `sizes` = the shards'
+    element counts, host integers) as an int64 tensor."""
+    parts = totals.numel()
+    dt = dtype_code(totals) if dtype is None else dtype
+    if out is None:
+        if op == OP_EXCLUSIVE_SCAN:
+            out = torch.empty(1, dtype=totals.dtype, device=totals.device)
+        else:
+            # uint64 on the device; int64 here (the offsets stay below 2^63)
+            out = torch.empty(2 if op == OP_PARTITION else 1, dtype=torch.int64,
+                              device=totals.device)
+    h = None
+    if sizes is not None:
+        h = (ctypes.c_uint64 * parts)(*[int(v) for v in sizes])
+    _check(load().gc_shard_offsets(op, dt, _ptr(totals), h, parts, rank, _ptr(out),
+                                   _stream(stream)), "gc_shard_offsets")
+    return out
+
+
+def exclusive_scan_carry(x: torch.Tensor, carry: torch.Tensor, out: torch.Tensor | None = None,
+                         total: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                         stream=None, with_total: bool = True):
+    """-> (out, total): out[i] = carry + x[0] + ... + x[i-1], total = carry + sum(x)."""
+    n = x.numel()
+    dt = dtype_code(x)
+    if out is None:
+        out = torch.empty_like(x)
+    if total is None and with_total:
+        total = torch.empty(1, dtype=x.dtype, device=x.device)
+    ws = _ws(ws, OP_EXCLUSIVE_SCAN, n, dt, x.device)
+    _check(load().gc_exclusive_scan_carry(_ptr(x), _ptr(out), _ptr(total), n, dt, _ptr(carry),
+                                          _ptr(ws), ws.numel(), _stream(stream)),
+           "gc_exclusive_scan_carry")
+    return out, total
+
+
+def select_if_at(x: torch.Tensor, pred, out: torch.Tensor, base: torch.Tensor,
+                 count: torch.Tensor | None = None, ws: torch.Tensor | None = None, stream=None):
+    """Survivors of x to out[base + rank] (out: the whole output; base: a
+    1-element uint64 device tensor) -> (out, count of this call)."""
+    n = x.numel()
+    dt = dtype_code(x)
+    if count is None:
+        count = torch.empty(1, dtype=torch.uint32, device=x.device)
+    ws = _ws(ws, OP_SELECT_IF, n, dt, x.device)
+    _check(load().gc_select_if_at(_ptr(x), _ptr(out), out.numel(), _ptr(base), _ptr(count), n, dt,
+                                  pred_code(pred), _ptr(ws), ws.numel(), _stream(stream)),
+           "gc_select_if_at")
+    return out, count
+
+
+def partition_at(x: torch.Tensor, pred, out: torch.Tensor, offsets: torch.Tensor,
+                 count_true: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                 stream=None):
+    """One shard of a partition into the whole output (offsets: the two uint64
+    of shard_offsets) -> (out, this shard's kept count)."""
+    n = x.numel()
+    dt = dtype_code(x)
+    if count_true is None:
+        count_true = torch.empty(1, dtype=torch.uint32, device=x.device)
+    ws = _ws(ws, OP_PARTITION, n, dt, x.device)
+    _check(load().gc_partition_at(_ptr(x), _ptr(out), out.numel(), _ptr(offsets), _ptr(count_true),
+                                  n, dt, pred_code(pred), _ptr(ws), ws.numel(), _stream(stream)),
+           "gc_partition_at")
+    return out, count_true

@@ -222,3 +222,52 @@ def test_binding_refuses_cpu_tensors(lib):
         gc.exclusive_scan(x, out=x.clone(), ws=torch.zeros(4096, dtype=torch.uint8))
     with pytest.raises(TypeError):
         gc.dtype_code(torch.zeros(3, dtype=torch.int64))
+
+
+def test_shard_entry_point_validation(lib):
+    """The sharded entry points reject bad arguments on the host."""
+    import ctypes
+    E = {v: k for k, v in gc.STATUS.items()}
+    V = ctypes.c_void_p
+    f = lib.gc_reduce
+    f.argtypes = [V, V, ctypes.c_size_t, ctypes.c_int, V, ctypes.c_size_t, V]
+    assert f(IN, None, 1000, gc.I32, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+    assert f(IN, CNT + 2, 1000, gc.I32, WS, BIG, None) == E["GC_ERR_MISALIGNED"]
+    assert f(IN, IN + 40, 1000, gc.I32, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]  # total in input
+    assert f(IN, CNT, 1000, 9, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+    f = lib.gc_count_if
+    f.argtypes = [V, V, ctypes.c_size_t, ctypes.c_int, ctypes.c_int, V, ctypes.c_size_t, V]
+    assert f(IN, CNT, 1000, gc.F32, gc.ODD, WS, BIG, None) == E["GC_ERR_UNSUPPORTED"]
+    assert f(IN, None, 1000, gc.I32, gc.ODD, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+    f = lib.gc_exclusive_scan_carry
+    f.argtypes = [V, V, V, ctypes.c_size_t, ctypes.c_int, V, V, ctypes.c_size_t, V]
+    assert f(IN, OUT, None, 1000, gc.I32, None, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+    assert f(IN, OUT, None, 1000, gc.I32, CNT + 1, WS, BIG, None) == E["GC_ERR_MISALIGNED"]
+    assert f(IN, OUT, None, 1000, gc.I32, OUT + 8, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+    f = lib.gc_select_if_at
+    f.argtypes = [V, V, ctypes.c_size_t, V, V, ctypes.c_size_t, ctypes.c_int, ctypes.c_int, V,
+                  ctypes.c_size_t, V]
+    assert f(IN, OUT, 5000, None, CNT, 1000, gc.I32, gc.ODD, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+    assert f(IN, OUT, 5000, CNT + 4, CNT, 1000, gc.I32, gc.ODD, WS, BIG, None) == E["GC_ERR_MISALIGNED"]
+    assert f(IN, OUT, 0, CNT + 8, CNT, 1000, gc.I32, gc.ODD, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+    # the whole output (capacity) must not overlap the input
+    assert f(IN, IN - 4 * 100, 5000, CNT + 8, CNT, 1000, gc.I32, gc.ODD, WS, BIG, None) == \
+        E["GC_ERR_INVALID_VALUE"]
+    f = lib.gc_partition_at
+    f.argtypes = [V, V, ctypes.c_size_t, V, V, ctypes.c_size_t, ctypes.c_int, ctypes.c_int, V,
+                  ctypes.c_size_t, V]
+    assert f(IN, OUT, 999, CNT + 8, CNT, 1000, gc.I32, gc.ODD, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+    assert f(IN, OUT, 5000, None, CNT, 1000, gc.I32, gc.ODD, WS, BIG, None) == E["GC_ERR_INVALID_VALUE"]
+    f = lib.gc_shard_offsets
+    U64P = ctypes.POINTER(ctypes.c_uint64)
+    f.argtypes = [ctypes.c_int, ctypes.c_int, V, U64P, ctypes.c_size_t, ctypes.c_size_t, V, V]
+    sizes = (ctypes.c_uint64 * 4)(1, 2, 3, 4)
+    assert f(gc.OP_SELECT_IF, gc.U32, CNT, None, 4, 4, OUT, None) == E["GC_ERR_INVALID_VALUE"]   # rank >= parts
+    assert f(gc.OP_SELECT_IF, gc.U32, CNT, None, 0, 0, OUT, None) == E["GC_ERR_INVALID_VALUE"]   # no parts
+    assert f(gc.OP_PARTITION, gc.U32, CNT, None, 4, 1, OUT, None) == E["GC_ERR_INVALID_VALUE"]   # sizes needed
+    assert f(gc.OP_RADIX_SORT, gc.U32, CNT, sizes, 4, 1, OUT, None) == E["GC_ERR_INVALID_VALUE"]
+    assert f(gc.OP_SELECT_IF, gc.U32, CNT, None, 4, 1, OUT + 4, None) == E["GC_ERR_MISALIGNED"]
+    big = (ctypes.c_uint64 * 2)(1, 1 << 31)
+    assert f(gc.OP_PARTITION, gc.U32, CNT, big, 2, 1, OUT, None) == E["GC_ERR_INVALID_VALUE"]
+    for op in (gc.OP_REDUCE, gc.OP_COUNT_IF):
+        assert lib.gc_workspace_bytes(op, 1 << 20, gc.I32) >= 512
