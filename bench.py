@@ -73,6 +73,9 @@ def parse_args(argv=None):
                    help="elements per array in the timed CPU-oracle sample")
     p.add_argument("--configs", action="store_true",
                    help="instead of the step: one line per benchmark configuration at its own size")
+    p.add_argument("--kernels", action="store_true",
+                   help="instead of the step: every entry point once at n elements (a workload for "
+                        "an ncu launch list of every kernel), then one line per call with its bytes")
     return p.parse_args(argv)
 
 
@@ -916,8 +919,105 @@ def run_configs(args):
         "moves 8 + 4 * kept B/element: the pre-pass reads the input once more")
 
 
+# ---------------------------------------------------------------- every kernel once
+
+def run_kernels(args):
+    """Every entry point of the library once at n elements, on one stream, in
+    a fixed order, so that an ncu capture of this process lists every kernel
+    (the persistent pipelines for each op and predicate kind, the
+    one-tile-per-CTA kernels through pointers one element into their
+    allocations, the pre-passes, the comparators, the sorts and the sharded
+    calls).  Prints one JSON line per call: its name, kernels launched and
+    algorithmic bytes, for the summary of the capture."""
+    import torch
+
+    from partition_pass_tile_gb300 import gc, synth
+
+    n = args.n
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    s = torch.cuda.Stream(device=dev)
+    gc.load()
+
+    def to_dev(a, off=0):
+        base = a.view(np.int32) if a.dtype == np.uint32 else a
+        t = torch.from_numpy(base)
+        if off:
+            big = torch.zeros(t.numel() + off, dtype=t.dtype)
+            big[off:] = t
+            g = big.to(dev)[off:]
+        else:
+            g = t.to(dev)
+        return g.view(torch.uint32) if a.dtype == np.uint32 else g
+
+    x = synth.uniform_i32(n, 4)
+    f = synth.scan_unit_f32(n, 2)
+    y = synth.keep_fraction(n, 0.5, 42)
+    keys, vals = synth.radix_keys(n, 5)
+    xd, fd, yd = to_dev(x), to_dev(f), to_dev(y)
+    kd, vd = to_dev(keys), to_dev(vals)
+    xo, yo = to_dev(x, 1), to_dev(y, 1)  # 4-byte, not 16-byte aligned
+    out = torch.empty(n + 4, dtype=torch.int32, device=dev)
+    out2 = torch.empty(n + 4, dtype=torch.int32, device=dev)
+    o_al, o_mis = out[:n], out[1:n + 1]
+    cnt = torch.zeros(8, dtype=torch.uint32, device=dev)
+    ws = gc.workspace(gc.OP_RADIX_SORT, n, gc.F32, dev)
+    kept = int(np.count_nonzero(y))
+    sel_b = 4.0 * n + 4.0 * kept + 4
+    from partition_pass_tile_gb300 import shard
+    P = 4
+    bounds = [shard.shard_bounds(n, P, r) for r in range(P)]
+    totals = torch.empty(P, dtype=torch.int32, device=dev)
+    carry = torch.empty(1, dtype=torch.int32, device=dev)
+    pf = gc.predicate(fd, ">", 0.75)
+    calls = [
+        ("scan_i32", 1, 8.0 * n, lambda: gc.exclusive_scan(xd, out=o_al, total=cnt[0:1].view(torch.int32), ws=ws, stream=s)),
+        ("scan_f32", 1, 8.0 * n, lambda: gc.exclusive_scan(fd, out=o_al.view(torch.float32), total=cnt[0:1].view(torch.float32), ws=ws, stream=s)),
+        ("inclusive_scan_i32", 1, 8.0 * n, lambda: gc.inclusive_scan(xd, out=o_al, total=cnt[0:1].view(torch.int32), ws=ws, stream=s)),
+        ("select_p50", 1, sel_b, lambda: gc.select_if(yd, "nonzero", out=o_al, count=cnt[1:2], ws=ws, stream=s)),
+        ("select_pred_f32_gt_0.75", 1, None, lambda: gc.select_if_pred(fd, pf, out=o_al, count=cnt[1:2], ws=ws, stream=s)),
+        ("partition_even", 2, 8.0 * n, lambda: gc.partition(xd, "even", out=o_al, count_true=cnt[2:3], ws=ws, stream=s)),
+        ("partition_pred_i32_lt_0", 2, 8.0 * n, lambda: gc.partition_pred(xd, gc.predicate(xd, "<", 0), out=o_al, count_true=cnt[2:3], ws=ws, stream=s)),
+        ("atomic_per_survivor_p50", 1, sel_b, lambda: gc.select_if_atomic(yd, "nonzero", out=o_al, count=cnt[3:4], ws=ws, stream=s)),
+        ("atomic_per_tile_p50", 1, sel_b, lambda: gc.select_if_atomic(yd, "nonzero", out=o_al, count=cnt[3:4], ws=ws, stream=s, per_tile=True)),
+        ("misaligned_scan_i32", 1, 8.0 * n, lambda: gc.exclusive_scan(xo, out=o_mis, total=cnt[0:1].view(torch.int32), ws=ws, stream=s)),
+        ("misaligned_select_p50", 1, sel_b, lambda: gc.select_if(yo, "nonzero", out=o_mis, count=cnt[1:2], ws=ws, stream=s)),
+        ("misaligned_partition_even", 2, 8.0 * n, lambda: gc.partition(xo, "even", out=o_mis, count_true=cnt[2:3], ws=ws, stream=s)),
+        ("reduce_i32", 1, 4.0 * n, lambda: gc.reduce(xd, total=totals[0:1], ws=ws, stream=s)),
+        ("count_if_even", 1, 4.0 * n, lambda: gc.count_if(xd, "even", count=cnt[4:5], ws=ws, stream=s)),
+        ("shard_offsets", 1, 0.0, lambda: gc.shard_offsets(gc.OP_EXCLUSIVE_SCAN, totals, 2, out=carry, stream=s)),
+        ("scan_carry_i32", 1, 8.0 * n, lambda: gc.exclusive_scan_carry(xd, carry, out=o_al, with_total=False, ws=ws, stream=s)),
+        ("split_radix_1bit", 2, 16.0 * n + 4.0 * n, lambda: gc.split_radix(kd, vd, 0, 1, keys_out=o_al.view(torch.uint32), vals_out=out2[:n].view(torch.uint32), ws=ws, stream=s)),
+        ("radix_sort_u32_digits", 12, 64.0 * n, lambda: gc.radix_sort(kd, vd, keys_out=o_al.view(torch.uint32), vals_out=out2[:n].view(torch.uint32), ws=ws, stream=s)),
+    ]
+    for name, launches, nbytes, fn in calls:
+        fn()
+        torch.cuda.synchronize(dev)
+        if nbytes is None:
+            m = int(cnt[1:2].view(torch.int32).item())
+            nbytes = 4.0 * n + 4.0 * m + 4
+        print(json.dumps({"call": name, "n": n, "launches": launches, "alg_bytes": nbytes}), flush=True)
+    # the placed passes of one shard (shard 2 of 4), as the first shard of
+    # its own output: base 0, and the partition's rejected run from T
+    a, b = bounds[2]
+    base = torch.zeros(1, dtype=torch.int64, device=dev)
+    gc.select_if_at(yd[a:b], "nonzero", o_al, base, count=cnt[6:7], ws=ws, stream=s)
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"call": "select_at_shard", "n": b - a, "launches": 1,
+                      "alg_bytes": 4.0 * (b - a) + 4.0 * int(cnt[6:7].view(torch.int32).item())}), flush=True)
+    gc.count_if(xd[a:b], "even", count=cnt[5:6], ws=ws, stream=s)
+    offs = gc.shard_offsets(gc.OP_PARTITION, cnt[5:6], 0, sizes=[b - a], dtype=gc.U32, stream=s)
+    gc.partition_at(xd[a:b], "even", o_al, offs, count_true=cnt[7:8], ws=ws, stream=s)
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"call": "partition_at_shard", "n": b - a, "launches": 3, "alg_bytes": 8.0 * (b - a)}),
+          flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.kernels:
+        run_kernels(args)
+        return
     if args.configs:
         run_configs(args)
         return

@@ -179,9 +179,12 @@ gc_status gc_workspace_init(void *d_ws, size_t ws_bytes, cudaStream_t stream);
  * tile in float32 with round-to-nearest and carries the running prefix
  * between tiles as an unevaluated pair of float32 values (about 48
  * significant bits; the kernel for pointers that are not 16-byte aligned
- * carries a float64), and each output is hi + (lo + the in-tile sum), so the
- * result is within a few float32 ulps of the exact prefix; the summation
- * order is not sequential.
+ * carries a float64); the sums of the tiles between a CTA's consecutive
+ * tiles are added in float32.  Each output is the prefix of its 4-element
+ * vector, rounded to float32, plus the sum of the vector's earlier elements,
+ * so the result is within a few float32 roundings of the exact prefix
+ * (relative error below 1e-6 for non-negative inputs); the summation order
+ * is not sequential.
  */
 gc_status gc_exclusive_scan(const void *d_in, void *d_out, void *d_total,
                             size_t n, gc_dtype dtype, void *d_ws,

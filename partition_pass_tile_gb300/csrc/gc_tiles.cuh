@@ -64,42 +64,35 @@ __device__ __forceinline__ void ff_add(float ah, float al, float bh, float bl, f
     fast_two_sum(s, e, sh, sl);
 }
 
-// Window of float32 aggregates summed as an unevaluated float pair
-// (double-float arithmetic, about 48 significant bits), per thread, across
-// the warp and across the CTA; every thread gets the pair.  No double
-// arithmetic: it is slow on this GPU.
+// Window of float32 aggregates summed in float32, per thread, across the
+// warp (a butterfly) and across the CTA; every thread gets the sum.  At most
+// two adds per thread, five in the warp and W - 1 across warps: the relative
+// error of the window stays below about 14 float32 roundings (1e-6), and the
+// window is added to a running prefix that is carried as a float pair, so
+// the error does not grow with the number of tiles.
 template <int THREADS>
-__device__ __forceinline__ void window_finish_ff(const uint64_t *status, uint32_t lo, uint32_t hi,
-                                                 WindowLoads &wl, uint8_t *ws, uint32_t tile,
-                                                 uint64_t timeout_ns, float *s_hi, float *s_lo,
-                                                 float &out_hi, float &out_lo)
+__device__ __forceinline__ float window_finish_f32(const uint64_t *status, uint32_t lo, uint32_t hi,
+                                                   WindowLoads &wl, uint8_t *ws, uint32_t tile,
+                                                   uint64_t timeout_ns, float *s_win)
 {
-    float sh = 0.0f, sl = 0.0f;
+    float sum = 0.0f;
 #pragma unroll
     for (int i = 0; i < kWinPerThread; ++i) {
         const uint32_t j = lo + threadIdx.x + uint32_t(i) * THREADS;
         if (j < hi) {
             uint32_t v = uint32_t(wl.w[i]);
             if (uint32_t(wl.w[i] >> 32) == kFlagNone) v = await_aggregate(status, j, ws, tile, timeout_ns);
-            ff_add(sh, sl, __uint_as_float(v), 0.0f, sh, sl);
+            sum += __uint_as_float(v);
         }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float oh = __shfl_xor_sync(kFullMask, sh, o);
-        const float ol = __shfl_xor_sync(kFullMask, sl, o);
-        ff_add(sh, sl, oh, ol, sh, sl);
-    }
-    if ((threadIdx.x & 31) == 0) {
-        s_hi[threadIdx.x >> 5] = sh;
-        s_lo[threadIdx.x >> 5] = sl;
-    }
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFullMask, sum, o);
+    if ((threadIdx.x & 31) == 0) s_win[threadIdx.x >> 5] = sum;
     __syncthreads();
-    float th = 0.0f, tl = 0.0f;
+    float t = 0.0f;
 #pragma unroll
-    for (int w = 0; w < THREADS / 32; ++w) ff_add(th, tl, s_hi[w], s_lo[w], th, tl);
-    out_hi = th;
-    out_lo = tl;
+    for (int w = 0; w < THREADS / 32; ++w) t += s_win[w];
+    return t;
 }
 
 // ---------------------------------------------------------------- the driver
@@ -134,7 +127,7 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
     constexpr uint32_t TE = Op::kTileElems;
     constexpr int W = THREADS / 32;
     __shared__ uint32_t s_win_u[W];
-    __shared__ float s_win_hi[W], s_win_lo[W];
+    __shared__ float s_win_hi[W];
     const P pipe{smem};
     const int tid = threadIdx.x;
     uint64_t *status = reinterpret_cast<uint64_t *>(ws + kStatusOff) + plan.region;
@@ -237,11 +230,10 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
                     op.template load<false>(pipe, ps, pbase, pstaged, n, prev_agg, ld);
             }
             if constexpr (Op::kF32) {
-                float wh, wl_;
-                window_finish_ff<THREADS>(status, window_lo(prev), prev, wl, ws, prev, timeout_ns,
-                                          s_win_hi, s_win_lo, wh, wl_);
+                const float wsum = window_finish_f32<THREADS>(status, window_lo(prev), prev, wl, ws,
+                                                              prev, timeout_ns, s_win_hi);
                 float ph, pl;
-                ff_add(run_h, run_l, wh, wl_, ph, pl);  // prefix(p) = run + window
+                ff_add(run_h, run_l, wsum, 0.0f, ph, pl);  // prefix(p) = run + window
                 ff_add(ph, pl, __uint_as_float(prev_agg), 0.0f, run_h, run_l);
                 if (full)
                     op.template finish_f32<true>(pipe, ps, pbase, pstaged, n, ph, pl, last, run_h + run_l, prv, ld);
@@ -396,9 +388,10 @@ struct ScanOp {
         (void)tile;
     }
 
-    // float32: each output is hi + (lo + local), with hi + lo the tile's
-    // exclusive prefix (a float pair carrying about 48 significant bits) and
-    // local the float sum inside the tile.
+    // float32: hi + lo is the tile's exclusive prefix, a float pair carrying
+    // about 48 significant bits; each vector's prefix is hi + (lo + its
+    // offset inside the tile), rounded once, and each output adds the sum of
+    // the vector's elements before it.
     template <bool FULL, class P>
     __device__ __forceinline__ void finish_f32(const P &pipe, int s, uint32_t base, uint32_t staged,
                                                uint32_t n, float hi, float lo, bool last,
@@ -428,13 +421,23 @@ struct ScanOp {
         __syncthreads();
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) {
-            float local = s_chunk[r * TT::kWarps + warp] + lane_excl[r];
+            // the vector's exclusive prefix, once per vector; then each
+            // output is that plus the sum inside the vector (one add)
+            const float vbase = hi + (lo + (s_chunk[r * TT::kWarps + warp] + lane_excl[r]));
+            const float a0 = __uint_as_float(x[r][0]), a1 = __uint_as_float(x[r][1]);
+            const float a2 = __uint_as_float(x[r][2]), a3 = __uint_as_float(x[r][3]);
+            const float s1 = a0 + a1, s2 = s1 + a2;
             uint32_t o[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (INCL) local += __uint_as_float(x[r][q]);
-                o[q] = __float_as_uint(hi + (lo + local));
-                if (!INCL) local += __uint_as_float(x[r][q]);
+            if (INCL) {
+                o[0] = __float_as_uint(vbase + a0);
+                o[1] = __float_as_uint(vbase + s1);
+                o[2] = __float_as_uint(vbase + s2);
+                o[3] = __float_as_uint(vbase + (s2 + a3));
+            } else {
+                o[0] = __float_as_uint(vbase);
+                o[1] = __float_as_uint(vbase + a0);
+                o[2] = __float_as_uint(vbase + s1);
+                o[3] = __float_as_uint(vbase + s2);
             }
             store4<OUT_VEC && !FULL>(out, base + r * TT::kRowElems + 4 * tid, n, o, FULL && OUT_VEC);
         }
@@ -495,7 +498,7 @@ struct SelectPlacement {
 // that precedes the first write, and a survivor's rank never exceeds its
 // index), shifted so that shared and global addresses agree modulo 16 bytes,
 // then written as one contiguous run with 128-bit stores.
-template <int THREADS, int ROWS, class Pred, bool VEC>
+template <int THREADS, int ROWS, class Pred, bool VEC, bool PLACED = false>
 struct SelectOp {
     using TT = Tile<THREADS, ROWS>;
     static constexpr uint32_t kTileElems = TT::kElems;
@@ -549,14 +552,18 @@ struct SelectOp {
     {
         uint32_t *buf = pipe.buf(s);
         if (threadIdx.x == 0 && last) *count = before + kept;
-        // placed output: out[obase + before + rank], refused past cap
-        const uint64_t ob = place.obase != nullptr ? __ldg(place.obase) : 0ull;
-        if (ob + before + kept > place.cap) {
-            if (threadIdx.x == 0) record_error(ws, kDeviceCheckCode, tile);
-            return;
+        uint32_t *o = out;
+        uint32_t d0 = before;  // index into o
+        if constexpr (PLACED) {
+            // placed output: out[obase + before + rank], refused past cap
+            const uint64_t ob = __ldg(place.obase);
+            if (ob + before + kept > place.cap) {
+                if (threadIdx.x == 0) record_error(ws, kDeviceCheckCode, tile);
+                return;
+            }
+            o = out + (ob & ~3ull);
+            d0 = uint32_t(ob & 3ull) + before;
         }
-        uint32_t *const o = out + (ob & ~3ull);
-        const uint32_t d0 = uint32_t(ob & 3ull) + before;  // index into o
         if (kept < kSparse) {
             // Survivor q of vector r goes to before + base[r] + (survivors of
             // the vector before it); no shared-memory writes, so no barrier.

@@ -181,14 +181,23 @@ cudaError_t dispatch_select(const uint32_t *in, uint32_t *out, uint32_t *count, 
     if (gch::aligned16(in) && !o.skip_first_tile) {
         constexpr int PT = gch::kSelectPipeThreads, PR = gch::kSelectPipeRows;
         constexpr int PS = gch::kSelectPipeStages;
+        // The placed form (a shard of a larger select-if) is its own
+        // instantiation, so the plain select keeps its 32-bit addressing.
+        auto go = [&](auto op) {
+            op.srcs[0] = in;
+            op.out = out;
+            op.count = count;
+            op.pred = pred;
+            op.place = place;
+            op.ws = ws;
+            return gcd::launch_pipeline<PT, PS>(op, n, ws, s, o);
+        };
+        const bool vec = gch::aligned16(out), placed = place.obase != nullptr;
         cudaError_t e;
-        if (gch::aligned16(out)) {
-            gcd::SelectOp<PT, PR, Pred, true> op{{in}, out, count, pred, place, ws};
-            e = gcd::launch_pipeline<PT, PS>(op, n, ws, s, o);
-        } else {
-            gcd::SelectOp<PT, PR, Pred, false> op{{in}, out, count, pred, place, ws};
-            e = gcd::launch_pipeline<PT, PS>(op, n, ws, s, o);
-        }
+        if (placed)
+            e = vec ? go(gcd::SelectOp<PT, PR, Pred, true, true>{}) : go(gcd::SelectOp<PT, PR, Pred, false, true>{});
+        else
+            e = vec ? go(gcd::SelectOp<PT, PR, Pred, true, false>{}) : go(gcd::SelectOp<PT, PR, Pred, false, false>{});
         if (e == cudaSuccess) return e;
         (void)cudaGetLastError();  // cooperative grid refused: one tile per CTA instead
     }
