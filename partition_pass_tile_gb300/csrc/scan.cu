@@ -170,15 +170,24 @@ reduce_kernel(const uint32_t *__restrict__ in, uint32_t n, uint8_t *ws, uint32_t
     const uint32_t stride = gridDim.x * 256u;
     uint32_t su = 0u;
     float h = 0.0f, l = 0.0f;
-    for (uint32_t v = blockIdx.x * 256u + tid; v < nvec; v += stride) {
-        uint32_t x[4];
-        load4<VEC>(in, 4u * v, n, 0u, x);
-        if (F32) {
-            const float a = (__uint_as_float(x[0]) + __uint_as_float(x[1])) +
-                            (__uint_as_float(x[2]) + __uint_as_float(x[3]));
-            ff_add(h, l, a, 0.0f, h, l);
-        } else {
-            su += x[0] + x[1] + x[2] + x[3];
+    constexpr uint32_t kUnroll = 4;  // loads in flight per thread
+    for (uint32_t v0 = blockIdx.x * 256u + tid; v0 < nvec; v0 += kUnroll * stride) {
+        uint32_t x[kUnroll][4];
+#pragma unroll
+        for (uint32_t u = 0; u < kUnroll; ++u) {
+            const uint32_t v = v0 + u * stride;
+            if (v < nvec) load4<VEC>(in, 4u * v, n, 0u, x[u]);
+            else x[u][0] = x[u][1] = x[u][2] = x[u][3] = 0u;
+        }
+#pragma unroll
+        for (uint32_t u = 0; u < kUnroll; ++u) {
+            if (F32) {
+                const float a = (__uint_as_float(x[u][0]) + __uint_as_float(x[u][1])) +
+                                (__uint_as_float(x[u][2]) + __uint_as_float(x[u][3]));
+                ff_add(h, l, a, 0.0f, h, l);
+            } else {
+                su += x[u][0] + x[u][1] + x[u][2] + x[u][3];
+            }
         }
     }
     uint64_t *partial = reinterpret_cast<uint64_t *>(ws + kStatusOff);
@@ -213,21 +222,38 @@ reduce_kernel(const uint32_t *__restrict__ in, uint32_t n, uint8_t *ws, uint32_t
         s_last = atomicAdd(hdr_u32(ws, kHdrReduceCtr), 1u) == gridDim.x - 1u ? 1u : 0u;
     }
     __syncthreads();
-    if (s_last == 0u || tid != 0) return;
+    if (s_last == 0u) return;
+    // The last CTA adds the partials, every thread a strided share, then the
+    // CTA in warp order: a fixed order, so the total is the same every call.
     __threadfence();
+    __shared__ double s_d[W];
     if (F32) {
         double acc = 0.0;
-        for (uint32_t b = 0; b < gridDim.x; ++b) {
+        for (uint32_t b = tid; b < gridDim.x; b += 256u) {
             const uint64_t w = ld_relaxed_gpu(partial + b);
             acc += double(__uint_as_float(uint32_t(w))) + double(__uint_as_float(uint32_t(w >> 32)));
         }
-        *total = __float_as_uint(float(acc));
+        acc = warp_sum(acc);
+        if (lane == 0) s_d[warp] = acc;
     } else {
         uint32_t acc = 0u;
-        for (uint32_t b = 0; b < gridDim.x; ++b) acc += uint32_t(ld_relaxed_gpu(partial + b));
-        *total = acc;
+        for (uint32_t b = tid; b < gridDim.x; b += 256u) acc += uint32_t(ld_relaxed_gpu(partial + b));
+        acc = warp_sum(acc);
+        if (lane == 0) s_u[warp] = acc;
     }
-    atomicExch(hdr_u32(ws, kHdrReduceCtr), 0u);
+    __syncthreads();
+    if (tid == 0) {
+        if (F32) {
+            double t = 0.0;
+            for (int w = 0; w < W; ++w) t += s_d[w];
+            *total = __float_as_uint(float(t));
+        } else {
+            uint32_t t = 0u;
+            for (int w = 0; w < W; ++w) t += s_u[w];
+            *total = t;
+        }
+        atomicExch(hdr_u32(ws, kHdrReduceCtr), 0u);
+    }
 }
 
 }  // namespace
