@@ -45,8 +45,9 @@
  *
  *   - Pointers named d_* are device pointers (cudaMalloc / torch memory on
  *     the current device).  Element pointers must be 4-byte aligned; 16-byte
- *     aligned element pointers take the vectorised kernels, others a scalar
- *     variant of the same kernels with identical results.
+ *     aligned element pointers take the vectorised kernels, others the same
+ *     kernels with each tile staged from the 16-byte boundary below it and
+ *     outputs stored element by element, with identical results.
  *   - n is an element count, 0 <= n <= GC_MAX_ELEMENTS (2^31 - 1).
  *   - Every call is asynchronous on `stream` (0 = legacy default stream):
  *     it enqueues work and returns.  Counts and totals are written to device
@@ -178,8 +179,8 @@ gc_status gc_workspace_init(void *d_ws, size_t ws_bytes, cudaStream_t stream);
  * int32 and uint32 add modulo 2^32 (the same bits).  float32 adds within a
  * tile in float32 with round-to-nearest and carries the running prefix
  * between tiles as an unevaluated pair of float32 values (about 48
- * significant bits; the kernel for pointers that are not 16-byte aligned
- * carries a float64); the sums of the tiles between a CTA's consecutive
+ * significant bits; the one-tile-per-CTA kernel run when the device
+ * refuses a cooperative grid carries a float64); the sums of the tiles between a CTA's consecutive
  * tiles are added in float32.  Each output is the prefix of its 4-element
  * vector, rounded to float32, plus the sum of the vector's earlier elements,
  * so the result is within a few float32 roundings of the exact prefix

@@ -36,8 +36,7 @@ gc_status gc_testing_select_if_skip_tile0(const void *d_in, void *d_out, uint32_
  * arrival counter the way a barrier wait that ran out leaves it, so no CTA
  * of this call ever sees the barrier complete.  Each CTA's wait gives up
  * after timeout_ns nanoseconds of device time, records GC_ERR_TIMEOUT and
- * carries on.  Requires a 16-byte-aligned d_in (the persistent kernel's
- * path) and n >= 1; otherwise GC_ERR_INVALID_VALUE, and argument errors as
+ * carries on.  Requires a 16-byte-aligned d_in and n >= 1; otherwise GC_ERR_INVALID_VALUE, and argument errors as
  * gc_exclusive_scan.  The output is undefined; gc_query_device_status then
  * returns GC_ERR_TIMEOUT and clears the barrier's words, after which the
  * workspace is fit for the next call.
@@ -61,6 +60,17 @@ gc_status gc_testing_select_if_noalloc_stalled_barrier(const void *d_in, void *d
                                                        gc_dtype dtype, gc_pred pred,
                                                        uint64_t timeout_ns,
                                                        cudaStream_t stream);
+
+/*
+ * Process-wide switch: while on is non-zero, every scan, select-if and
+ * partition (the one-bit split included) runs its one-tile-per-CTA kernels
+ * (dynamic tile ids, a warp look-back, a memset of the tile counter and
+ * status words first), which otherwise run only when the device refuses a
+ * cooperative grid.  The results are the same; tests use it to keep those
+ * kernels covered.  Not thread-safe with respect to calls in flight on other
+ * host threads.
+ */
+void gc_testing_force_fallback(int on);
 
 #ifdef __cplusplus
 }

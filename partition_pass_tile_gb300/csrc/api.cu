@@ -2,6 +2,7 @@
 // workspace sizing, and dispatch to the launchers.  Nothing here touches the
 // GPU before every argument has been checked, so argument errors are
 // reported without any CUDA call.
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -27,6 +28,10 @@ cudaError_t clear_accumulators(uint8_t *ws, cudaStream_t s)
     // header is scratch (the barrier's epoch among it: any value will do).
     return cudaMemsetAsync(ws + 8, 0, kHdrBarArrive - 8, s);
 }
+
+static std::atomic<bool> g_force_fallback{false};
+
+bool force_fallback() { return g_force_fallback.load(std::memory_order_relaxed); }
 
 int sm_count()
 {
@@ -606,6 +611,8 @@ gc_status gc_testing_select_if_skip_tile0(const void *d_in, void *d_out, uint32_
     return select_like(SelectKind::Stable, d_in, d_out, d_count, n, dtype, pred, d_ws, ws_bytes,
                        stream, o);
 }
+
+void gc_testing_force_fallback(int on) { g_force_fallback.store(on != 0); }
 
 gc_status gc_testing_exclusive_scan_stalled_barrier(const void *d_in, void *d_out, void *d_total,
                                                     size_t n, gc_dtype dtype, void *d_ws,

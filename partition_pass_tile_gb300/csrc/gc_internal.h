@@ -222,6 +222,11 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 int sm_count();  // multiprocessors of the current device (cached per device)
 
+// Test hook (gc_testing_force_fallback): when set, every scan, select-if
+// and partition runs the one-tile-per-CTA kernels, which otherwise run only
+// when the device refuses a cooperative grid.
+bool force_fallback();
+
 // Grid of a persistent kernel: as many CTAs as fit on the device at once
 // (never more than there are tiles).  Raises the kernel's dynamic shared
 // memory limit to `smem` first.  Returns <= 0 on failure.

@@ -194,10 +194,21 @@ struct Pipe {
     static constexpr uint32_t kBytes = kBarOff + 8u * STAGES;
 
     uint8_t *base;
+    // Elements by which each input array's pointer lies past a 16-byte
+    // boundary (0 .. 3).  A shifted array is copied from that boundary, one
+    // vector longer, so element j of a tile sits at buf(s, a)[j + sh[a]].
+    uint32_t sh[ARRAYS];
 
+    // The stage buffer as written by the kernel (16-byte aligned: in-place
+    // compaction and bulk stores).
     __device__ __forceinline__ uint32_t *buf(int s, int array = 0) const
     {
         return reinterpret_cast<uint32_t *>(base + s * kStageBytes + array * kArrBytes);
+    }
+    // The stage buffer as read: element j of the tile at rbuf(s, a)[j].
+    __device__ __forceinline__ uint32_t *rbuf(int s, int array = 0) const
+    {
+        return buf(s, array) + sh[array];
     }
     __device__ __forceinline__ uint64_t *bar(int s) const
     {
@@ -217,12 +228,23 @@ struct Pipe {
                                           uint32_t tile_elems, uint32_t n) const
     {
         const uint32_t first = tile * tile_elems;
-        const uint32_t bytes = (min(tile_elems, n - first) & ~3u) * 4u;
-        if (bytes != 0u) {
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar(s), bytes * ARRAYS);
+        const uint32_t valid = min(tile_elems, n - first);
+        // An aligned array: its whole vectors (the ragged end is read from
+        // global memory).  A shifted one: from the 16-byte boundary below the
+        // tile's first element up to the one above its last, every byte of it
+        // in a 16-byte chunk that holds an element of the array.
+        uint32_t bytes[ARRAYS], total = 0u;
 #pragma unroll
-            for (int a = 0; a < ARRAYS; ++a) bulk_load(buf(s, a), srcs[a] + first, bytes, bar(s));
+        for (int a = 0; a < ARRAYS; ++a) {
+            bytes[a] = sh[a] == 0u ? (valid & ~3u) * 4u : ((valid + sh[a] + 3u) & ~3u) * 4u;
+            total += bytes[a];
+        }
+        if (total != 0u) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar(s), total);
+#pragma unroll
+            for (int a = 0; a < ARRAYS; ++a)
+                if (bytes[a] != 0u) bulk_load(buf(s, a), srcs[a] + first - sh[a], bytes[a], bar(s));
         } else {
             mbar_arrive(bar(s));
         }
@@ -260,11 +282,30 @@ __device__ __forceinline__ uint32_t staged_elems(uint32_t tile, uint32_t tile_el
 // was copied there, otherwise from global memory (elements at or past n read
 // as `fill`).  FULL: the whole tile is staged (every tile but a ragged last
 // one), so no test is needed.
-template <bool FULL = false>
+// SH: the kernel instance reads shifted stages (an input pointer that is not
+// 16-byte aligned, sbuf = rbuf); its stage reads find the shift from sbuf's
+// address, and an aligned kernel instance has no such test at all.
+template <bool FULL = false, bool SH = false>
 __device__ __forceinline__ void stage_load4(const uint32_t *sbuf, const uint32_t *__restrict__ gin,
                                             uint32_t base, uint32_t li, uint32_t staged, uint32_t n,
                                             uint32_t fill, uint32_t (&v)[4])
 {
+    // A shifted stage: two aligned vectors, and the four words of the element
+    // vector.
+    const uint32_t sh = SH ? (smem_addr(sbuf) >> 2) & 3u : 0u;
+    if (SH && sh != 0u && (FULL || li + 4u <= staged)) {
+        const uint32_t *al = sbuf - sh;
+        const uint4 a = *reinterpret_cast<const uint4 *>(al + li);
+        const uint4 b = *reinterpret_cast<const uint4 *>(al + li + 4u);
+        if (sh == 1u) {
+            v[0] = a.y; v[1] = a.z; v[2] = a.w; v[3] = b.x;
+        } else if (sh == 2u) {
+            v[0] = a.z; v[1] = a.w; v[2] = b.x; v[3] = b.y;
+        } else {
+            v[0] = a.w; v[1] = b.x; v[2] = b.y; v[3] = b.z;
+        }
+        return;
+    }
     if (FULL || li + 4u <= staged) {
         const uint4 q = *reinterpret_cast<const uint4 *>(sbuf + li);
         v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;

@@ -128,7 +128,10 @@ __device__ __forceinline__ void pipeline_run(const Op &op, uint8_t *smem, uint32
     constexpr int W = THREADS / 32;
     __shared__ uint32_t s_win_u[W];
     __shared__ float s_win_hi[W];
-    const P pipe{smem};
+    P pipe{smem};
+#pragma unroll
+    for (int a = 0; a < int(sizeof(op.srcs) / sizeof(op.srcs[0])); ++a)
+        pipe.sh[a] = uint32_t(reinterpret_cast<uintptr_t>(op.srcs[a]) >> 2) & 3u;
     const int tid = threadIdx.x;
     uint64_t *status = reinterpret_cast<uint64_t *>(ws + kStatusOff) + plan.region;
 
@@ -269,19 +272,28 @@ constexpr int pipeline_max_grid() { return kWinPerThread * THREADS + 1; }
 
 // ---------------------------------------------------------------- tile bodies
 
+// The stage buffer as an op reads it: the shifted view when its input may
+// not be 16-byte aligned (SH), the buffer itself otherwise.
+template <bool SH, class P>
+__device__ __forceinline__ uint32_t *stage_rd(const P &pipe, int s, int array = 0)
+{
+    if constexpr (SH) return pipe.rbuf(s, array);
+    else return pipe.buf(s, array);
+}
+
 // The vectors of one staged tile.
-template <class TT, bool FULL>
+template <class TT, bool FULL, bool SH = false>
 __device__ __forceinline__ void tile_vectors(const uint32_t *sbuf, const uint32_t *gin,
                                              uint32_t base, uint32_t staged, uint32_t n,
                                              uint32_t (&x)[TT::kRows][4])
 {
 #pragma unroll
     for (int r = 0; r < TT::kRows; ++r)
-        stage_load4<FULL>(sbuf, gin, base, r * TT::kRowElems + 4 * threadIdx.x, staged, n, 0u, x[r]);
+        stage_load4<FULL, SH>(sbuf, gin, base, r * TT::kRowElems + 4 * threadIdx.x, staged, n, 0u, x[r]);
 }
 
 // Exclusive scan, uint32 (int32 bits) or float32.
-template <int THREADS, int ROWS, bool F32, bool OUT_VEC, bool INCL = false>
+template <int THREADS, int ROWS, bool F32, bool OUT_VEC, bool INCL = false, bool SH = false>
 struct ScanOp {
     using TT = Tile<THREADS, ROWS>;
     static constexpr uint32_t kTileElems = TT::kElems;
@@ -325,7 +337,7 @@ struct ScanOp {
 #pragma unroll
             for (int r = 0; r < ROWS; ++r) {
                 uint32_t x[4];
-                stage_load4<FULL>(pipe.buf(s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x);
+                stage_load4<FULL, SH>(stage_rd<SH>(pipe, s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x);
                 a += (__uint_as_float(x[0]) + __uint_as_float(x[1])) +
                      (__uint_as_float(x[2]) + __uint_as_float(x[3]));
             }
@@ -337,7 +349,7 @@ struct ScanOp {
 #pragma unroll
             for (int r = 0; r < ROWS; ++r) {
                 uint32_t x[4];
-                stage_load4<FULL>(pipe.buf(s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x);
+                stage_load4<FULL, SH>(stage_rd<SH>(pipe, s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x);
                 a += x[0] + x[1] + x[2] + x[3];
             }
             const uint32_t agg = block_sum_all<THREADS>(a, s_red);
@@ -358,7 +370,7 @@ struct ScanOp {
         uint32_t lane_excl[ROWS];
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) {
-            stage_load4<FULL>(pipe.buf(s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x[r]);
+            stage_load4<FULL, SH>(stage_rd<SH>(pipe, s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x[r]);
             const uint32_t v = x[r][0] + x[r][1] + x[r][2] + x[r][3];
             uint32_t incl = v;
 #pragma unroll
@@ -403,7 +415,7 @@ struct ScanOp {
         float lane_excl[ROWS];
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) {
-            stage_load4<FULL>(pipe.buf(s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x[r]);
+            stage_load4<FULL, SH>(stage_rd<SH>(pipe, s), srcs[0], base, r * TT::kRowElems + 4 * tid, staged, n, 0u, x[r]);
             const float v = (__uint_as_float(x[r][0]) + __uint_as_float(x[r][1])) +
                             (__uint_as_float(x[r][2]) + __uint_as_float(x[r][3]));
             float incl = v;
@@ -447,7 +459,7 @@ struct ScanOp {
 
 // Predicate masks of one staged tile: bit q of mask[r] says element q of
 // the thread's vector r is kept (and lies below n).
-template <class TT, bool FULL, class Pred>
+template <class TT, bool FULL, bool SH, class Pred>
 __device__ __forceinline__ void tile_masks(const uint32_t *sbuf, const uint32_t *gin, uint32_t base,
                                            uint32_t staged, uint32_t n, const Pred &pred,
                                            uint32_t (&mask)[TT::kRows])
@@ -457,7 +469,7 @@ __device__ __forceinline__ void tile_masks(const uint32_t *sbuf, const uint32_t 
     for (int r = 0; r < TT::kRows; ++r) {
         const uint32_t li = r * TT::kRowElems + 4 * tid;
         uint32_t x[4];
-        stage_load4<FULL>(sbuf, gin, base, li, staged, n, 0u, x);
+        stage_load4<FULL, SH>(sbuf, gin, base, li, staged, n, 0u, x);
         uint32_t m = 0u;
 #pragma unroll
         for (int q = 0; q < 4; ++q) m |= uint32_t((FULL || base + li + q < n) && pred(x[q])) << q;
@@ -467,14 +479,14 @@ __device__ __forceinline__ void tile_masks(const uint32_t *sbuf, const uint32_t 
 
 // Reduction of a predicate tile: masks, in-tile ranks and the keep count.
 // base[r] = survivors of the tile before this thread's vector r.
-template <class TT, bool FULL, class Pred, class OnTotal>
+template <class TT, bool FULL, bool SH, class Pred, class OnTotal>
 __device__ __forceinline__ uint32_t rank_tile(const uint32_t *sbuf, const uint32_t *gin,
                                               uint32_t base, uint32_t staged, uint32_t n,
                                               const Pred &pred, uint32_t (&mask)[TT::kRows],
                                               uint32_t (&rbase)[TT::kRows], const OnTotal &on_total)
 {
     __shared__ uint32_t s_chunk[TT::kChunks];
-    tile_masks<TT, FULL>(sbuf, gin, base, staged, n, pred, mask);
+    tile_masks<TT, FULL, SH>(sbuf, gin, base, staged, n, pred, mask);
     uint32_t lane_excl[TT::kRows];
     rank_masks<TT>(mask, lane_excl, s_chunk);
     __syncthreads();
@@ -498,7 +510,7 @@ struct SelectPlacement {
 // that precedes the first write, and a survivor's rank never exceeds its
 // index), shifted so that shared and global addresses agree modulo 16 bytes,
 // then written as one contiguous run with 128-bit stores.
-template <int THREADS, int ROWS, class Pred, bool VEC, bool PLACED = false>
+template <int THREADS, int ROWS, class Pred, bool VEC, bool PLACED = false, bool SH = false>
 struct SelectOp {
     using TT = Tile<THREADS, ROWS>;
     static constexpr uint32_t kTileElems = TT::kElems;
@@ -530,7 +542,7 @@ struct SelectOp {
                                                uint32_t n, Carry &c, const Publish &publish) const
     {
         // The count goes out before the per-row ranks are derived.
-        return rank_tile<TT, FULL>(pipe.buf(s), srcs[0], base, staged, n, pred, c.mask, c.base, publish);
+        return rank_tile<TT, FULL, SH>(stage_rd<SH>(pipe, s), srcs[0], base, staged, n, pred, c.mask, c.base, publish);
     }
 
     // A tile with fewer survivors than this skips the in-place compaction:
@@ -541,7 +553,7 @@ struct SelectOp {
     __device__ __forceinline__ void load(const P &pipe, int s, uint32_t base, uint32_t staged,
                                          uint32_t n, uint32_t kept, Loaded &ld) const
     {
-        if (kept >= kSparse) tile_vectors<TT, FULL>(pipe.buf(s), srcs[0], base, staged, n, ld.x);
+        if (kept >= kSparse) tile_vectors<TT, FULL, SH>(stage_rd<SH>(pipe, s), srcs[0], base, staged, n, ld.x);
     }
 
     template <bool FULL, class P>
@@ -550,7 +562,8 @@ struct SelectOp {
                                            uint32_t kept, bool last, const Carry &c,
                                            const Loaded &ld) const
     {
-        uint32_t *buf = pipe.buf(s);
+        uint32_t *buf = pipe.buf(s);          // written: in-place compaction
+        const uint32_t *rbuf = stage_rd<SH>(pipe, s);  // read: element j at rbuf[j]
         if (threadIdx.x == 0 && last) *count = before + kept;
         uint32_t *o = out;
         uint32_t d0 = before;  // index into o
@@ -575,7 +588,7 @@ struct SelectOp {
                 while (m != 0u) {
                     const uint32_t q = uint32_t(__ffs(m) - 1);
                     m &= m - 1u;
-                    const uint32_t x = (FULL || li + 4u <= staged) ? buf[li + q] : srcs[0][base + li + q];
+                    const uint32_t x = (FULL || li + 4u <= staged) ? rbuf[li + q] : srcs[0][base + li + q];
                     __stcs(o + pos, x);
                     ++pos;
                 }
@@ -603,7 +616,7 @@ struct SelectOp {
 
 // Predicate masks of one staged tile: bit q of mask[r] says element q of
 // thread's vector r is kept (and lies below n).
-template <class TT, bool FULL, class Pred>
+template <class TT, bool FULL, bool SH, class Pred>
 __device__ __forceinline__ void tile_masks_x(const uint32_t *sbuf, const uint32_t *gin, uint32_t base,
                                            uint32_t staged, uint32_t n, const Pred &pred,
                                            uint32_t (&x)[TT::kRows][4], uint32_t (&mask)[TT::kRows])
@@ -612,7 +625,7 @@ __device__ __forceinline__ void tile_masks_x(const uint32_t *sbuf, const uint32_
 #pragma unroll
     for (int r = 0; r < TT::kRows; ++r) {
         const uint32_t li = r * TT::kRowElems + 4 * tid;
-        stage_load4<FULL>(sbuf, gin, base, li, staged, n, 0u, x[r]);
+        stage_load4<FULL, SH>(sbuf, gin, base, li, staged, n, 0u, x[r]);
         uint32_t m = 0u;
 #pragma unroll
         for (int q = 0; q < 4; ++q) m |= uint32_t((FULL || base + li + q < n) && pred(x[r][q])) << q;
@@ -622,14 +635,14 @@ __device__ __forceinline__ void tile_masks_x(const uint32_t *sbuf, const uint32_
 
 // Keep count of one staged tile, to every thread; the masks it finds are
 // left in `mask` for the tile's finish a round later.
-template <class TT, bool FULL, class Pred>
+template <class TT, bool FULL, bool SH, class Pred>
 __device__ __forceinline__ uint32_t tile_count(const uint32_t *sbuf, const uint32_t *gin,
                                                uint32_t base, uint32_t staged, uint32_t n,
                                                const Pred &pred, uint32_t *s_red,
                                                uint32_t (&mask)[TT::kRows])
 {
     uint32_t x[TT::kRows][4];
-    tile_masks_x<TT, FULL>(sbuf, gin, base, staged, n, pred, x, mask);
+    tile_masks_x<TT, FULL, SH>(sbuf, gin, base, staged, n, pred, x, mask);
     uint32_t c = 0u;
 #pragma unroll
     for (int r = 0; r < TT::kRows; ++r) c += __popc(mask[r]);
@@ -642,7 +655,7 @@ __device__ __forceinline__ uint32_t tile_count(const uint32_t *sbuf, const uint3
 // -- Day 33" (scatterPartition), with T the total kept from the pre-pass.
 // Both runs are compacted in place in the stage buffer(s) and written with
 // 128-bit stores.
-template <int THREADS, int ROWS, class Pred, bool VEC, bool VALS, bool PLACED = false>
+template <int THREADS, int ROWS, class Pred, bool VEC, bool VALS, bool PLACED = false, bool SH = false>
 struct PartitionOp {
     using TT = Tile<THREADS, ROWS>;
     static constexpr uint32_t kTileElems = TT::kElems;
@@ -681,7 +694,7 @@ struct PartitionOp {
                                                uint32_t n, Carry &c, const Publish &publish) const
     {
         __shared__ uint32_t s_red[TT::kWarps];
-        const uint32_t agg = tile_count<TT, FULL>(pipe.buf(s), srcs[0], base, staged, n, pred, s_red, c.mask);
+        const uint32_t agg = tile_count<TT, FULL, SH>(stage_rd<SH>(pipe, s), srcs[0], base, staged, n, pred, s_red, c.mask);
         publish(agg);
         return agg;
     }
@@ -694,16 +707,16 @@ struct PartitionOp {
     {
         __shared__ uint32_t s_chunk[TT::kChunks];
         const int tid = threadIdx.x, warp = tid >> 5;
-        uint32_t *kbuf = pipe.buf(s, 0);
+        uint32_t *kbuf = pipe.buf(s, 0);  // written: in-place compaction of both runs
         uint32_t *vbuf = pipe.buf(s, VALS ? 1 : 0);
         uint32_t x[ROWS][4], lane_excl[ROWS];
         uint32_t v[VALS ? ROWS : 1][4];
-        tile_vectors<TT, FULL>(kbuf, srcs[0], base, staged, n, x);
+        tile_vectors<TT, FULL, SH>(stage_rd<SH>(pipe, s, 0), srcs[0], base, staged, n, x);
         const uint32_t (&mask)[ROWS] = c.mask;
         if (VALS) {
 #pragma unroll
             for (int r = 0; r < ROWS; ++r)
-                stage_load4<FULL>(vbuf, srcs[VALS ? 1 : 0], base, r * TT::kRowElems + 4 * tid, staged,
+                stage_load4<FULL, SH>(stage_rd<SH>(pipe, s, VALS ? 1 : 0), srcs[VALS ? 1 : 0], base, r * TT::kRowElems + 4 * tid, staged,
                                   n, 0u, v[VALS ? r : 0]);
         }
         rank_masks<TT>(mask, lane_excl, s_chunk);

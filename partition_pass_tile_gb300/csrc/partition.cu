@@ -339,13 +339,18 @@ cudaError_t run_partition_pipe(const uint32_t *kin, const uint32_t *vin, uint32_
     // The placed form (a shard of a larger partition) is its own
     // instantiation, so the plain partition and the radix splits keep their
     // 32-bit addressing.
+    // Inputs that are not 16-byte aligned are staged shifted, with the runs
+    // stored element by element.
+    const bool shifted = !gch::aligned16(kin) || (VALS && !gch::aligned16(vin));
     if (pl.offsets != nullptr) {
         if constexpr (!VALS) {
+            if (shifted) return go(gcd::PartitionOp<PT, PR, Pred, false, VALS, true, true>{});
             if (vec) return go(gcd::PartitionOp<PT, PR, Pred, true, VALS, true>{});
             return go(gcd::PartitionOp<PT, PR, Pred, false, VALS, true>{});
         }
         return cudaErrorNotSupported;
     }
+    if (shifted) return go(gcd::PartitionOp<PT, PR, Pred, false, VALS, false, true>{});
     if (vec) return go(gcd::PartitionOp<PT, PR, Pred, true, VALS, false>{});
     return go(gcd::PartitionOp<PT, PR, Pred, false, VALS, false>{});
 }
@@ -360,7 +365,7 @@ cudaError_t run_partition_pass(const uint32_t *kin, const uint32_t *vin, uint32_
                                bool *piped = nullptr, const PartPlace &pl = PartPlace{})
 {
     if (piped != nullptr) *piped = false;
-    if (gch::aligned16(kin) && (!VALS || gch::aligned16(vin)) && !o.skip_first_tile) {
+    if (!o.skip_first_tile && !gch::force_fallback()) {
         cudaError_t e;
         if (split)
             e = run_partition_pipe<gch::kSplitPipeThreads, gch::kSplitPipeRows, gch::kSplitPipeStages,

@@ -287,12 +287,12 @@ uint32_t scan_tile_elems() { return tile_elems(kScanPipeThreads, kScanPipeRows);
 
 namespace {
 
-template <bool F32, bool OUT_VEC, bool INCL>
+template <bool F32, bool OUT_VEC, bool INCL, bool SH = false>
 cudaError_t launch_scan_pipe(const uint32_t *in, uint32_t *out, uint32_t *total, uint32_t n,
                              uint8_t *ws, cudaStream_t s, const LaunchOpts &o,
                              const uint32_t *carry)
 {
-    using Op = gcd::ScanOp<kScanPipeThreads, kScanPipeRows, F32, OUT_VEC, INCL>;
+    using Op = gcd::ScanOp<kScanPipeThreads, kScanPipeRows, F32, OUT_VEC, INCL, SH>;
     Op op{{in}, out, total, carry};
     return gcd::launch_pipeline<kScanPipeThreads, kScanPipeStages>(op, n, ws, s, o);
 }
@@ -306,9 +306,14 @@ cudaError_t launch_scan_impl(const void *in, void *out, void *total, uint32_t n,
     auto *t = static_cast<uint32_t *>(total);
     auto *c = static_cast<const uint32_t *>(carry);
     cudaError_t e;
-    if (aligned16(in) && !o.skip_first_tile) {
+    if (!o.skip_first_tile && !force_fallback()) {
         const bool ov = aligned16(out);
-        if (dt == GC_F32)
+        // An input that is not 16-byte aligned is staged shifted (and its
+        // outputs stored element by element).
+        if (!aligned16(in))
+            e = dt == GC_F32 ? launch_scan_pipe<true, false, INCL, true>(i, u, t, n, ws, s, o, c)
+                             : launch_scan_pipe<false, false, INCL, true>(i, u, t, n, ws, s, o, c);
+        else if (dt == GC_F32)
             e = ov ? launch_scan_pipe<true, true, INCL>(i, u, t, n, ws, s, o, c)
                    : launch_scan_pipe<true, false, INCL>(i, u, t, n, ws, s, o, c);
         else
@@ -320,8 +325,8 @@ cudaError_t launch_scan_impl(const void *in, void *out, void *total, uint32_t n,
         // co-residency.  Clear the launch error first.
         (void)cudaGetLastError();
     }
-    // Unaligned input (or the test hook): one tile per CTA, loads straight
-    // into registers.
+    // A refused cooperative launch (or a test hook): one tile per CTA, loads
+    // straight into registers.
     const uint32_t tile = tile_elems(kScanThreads, kScanRows);
     const uint32_t tiles = uint32_t(ceil_div(n, tile));
     e = reset_tiles(ws, tiles, s, o.skip_first_tile);

@@ -178,7 +178,7 @@ cudaError_t dispatch_select(const uint32_t *in, uint32_t *out, uint32_t *count, 
                             Pred pred, uint8_t *ws, cudaStream_t s, const gch::LaunchOpts &o,
                             SelectPlacement place)
 {
-    if (gch::aligned16(in) && !o.skip_first_tile) {
+    if (!o.skip_first_tile && !gch::force_fallback()) {
         constexpr int PT = gch::kSelectPipeThreads, PR = gch::kSelectPipeRows;
         constexpr int PS = gch::kSelectPipeStages;
         // The placed form (a shard of a larger select-if) is its own
@@ -194,7 +194,10 @@ cudaError_t dispatch_select(const uint32_t *in, uint32_t *out, uint32_t *count, 
         };
         const bool vec = gch::aligned16(out), placed = place.obase != nullptr;
         cudaError_t e;
-        if (placed)
+        if (!gch::aligned16(in))  // staged shifted, survivors stored element by element
+            e = placed ? go(gcd::SelectOp<PT, PR, Pred, false, true, true>{})
+                       : go(gcd::SelectOp<PT, PR, Pred, false, false, true>{});
+        else if (placed)
             e = vec ? go(gcd::SelectOp<PT, PR, Pred, true, true>{}) : go(gcd::SelectOp<PT, PR, Pred, false, true>{});
         else
             e = vec ? go(gcd::SelectOp<PT, PR, Pred, true, false>{}) : go(gcd::SelectOp<PT, PR, Pred, false, false>{});

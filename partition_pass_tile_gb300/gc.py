@@ -329,6 +329,14 @@ def testing_select_if_skip_tile0(x: torch.Tensor, pred, out, count, ws, timeout_
         ws.numel(), timeout_ns, _stream(stream)))
 
 
+def testing_force_fallback(on: bool) -> None:
+    """Test hook (include/gc_testing.h): one-tile-per-CTA kernels while on."""
+    f = load().gc_testing_force_fallback
+    f.argtypes = [ctypes.c_int]
+    f.restype = None
+    f(1 if on else 0)
+
+
 def testing_exclusive_scan_stalled_barrier(x: torch.Tensor, out, total, ws, timeout_ns: int,
                                            stream=None) -> int:
     """Test hook (include/gc_testing.h): returns the launch status."""

@@ -38,7 +38,7 @@ def rand(n, dt, kind="wide"):
 # ---------------------------------------------------------------- scan
 
 @pytest.mark.parametrize("dt", [gc.I32, gc.U32, gc.F32])
-@pytest.mark.parametrize("offset", [0, 1])
+@pytest.mark.parametrize("offset", [0, 1, 2, 3])
 def test_scan_sizes(orc, dt, offset):
     for n in sizes_for(gc.OP_EXCLUSIVE_SCAN):
         x = rand(n, dt)
@@ -108,7 +108,7 @@ def select_input(n, dt):
 
 
 @pytest.mark.parametrize("dt,pred", CASES)
-@pytest.mark.parametrize("offset", [0, 3])
+@pytest.mark.parametrize("offset", [0, 1, 2, 3])
 def test_select_sizes(orc, dt, pred, offset):
     for n in sizes_for(gc.OP_SELECT_IF):
         x = select_input(n, dt)
@@ -146,7 +146,7 @@ def test_select_float_special_values(orc):
 # ---------------------------------------------------------------- partition
 
 @pytest.mark.parametrize("dt,pred", CASES)
-@pytest.mark.parametrize("offset", [0, 2])
+@pytest.mark.parametrize("offset", [0, 1, 2, 3])
 def test_partition_sizes(orc, dt, pred, offset):
     for n in sizes_for(gc.OP_PARTITION):
         x = select_input(n, dt) if dt == gc.F32 else rand(n, dt, "wide")
@@ -160,7 +160,7 @@ def test_partition_sizes(orc, dt, pred, offset):
 
 # ---------------------------------------------------------------- radix
 
-@pytest.mark.parametrize("offset", [0, 1])
+@pytest.mark.parametrize("offset", [0, 1, 2, 3])
 def test_radix_full_sort(orc, offset):
     for n in [1, 2, 33, 4095, 4097, 100_003, 300_001]:
         keys = synth.uniform_u32(n, int(RNG.integers(1 << 30)))
@@ -308,3 +308,37 @@ def test_streams_and_empty_inputs():
     c.view(torch.int32).fill_(5)
     gc.partition(e, "odd", out=e.clone(), count_true=c)
     assert c.view(torch.int32).item() == 0
+
+
+# ---------------------------------------------------------------- one tile per CTA
+
+def test_fallback_kernels_match_oracle(orc):
+    """The one-tile-per-CTA kernels (run when the device refuses a cooperative
+    grid), forced by the test hook, on ragged sizes with aligned and offset
+    pointers: scan, select-if, partition and the one-bit split."""
+    gc.testing_force_fallback(True)
+    try:
+        for n in (1, 1000, 3 * 8192 + 611, 100_003):
+            for off in (0, 1, 2):
+                x = rand(n, gc.I32, "small")
+                out, tot = gc.exclusive_scan(dev(x, off), out=empty_like_offset(dev(x), (off + 1) % 4))
+                want, wt = orc.exclusive_scan(x)
+                assert np.array_equal(host(out), want) and host(tot)[0] == wt, (n, off)
+                xf = synth.scan_unit_f32(n, 3)
+                out, _ = gc.exclusive_scan(dev(xf, off))
+                assert f32_within(host(out), orc.exclusive_scan(xf)[0])[0].size == 0, (n, off)
+                y = select_input(n, gc.I32)
+                out, cnt = gc.select_if(dev(y, off), gc.ODD)
+                want = orc.select_if(y, gc.ODD)
+                m = int(host(cnt)[0])
+                assert m == want.shape[0] and np.array_equal(host(out)[:m], want), (n, off)
+                out, ct = gc.partition(dev(x, off), gc.EVEN)
+                want, t = orc.partition(x, gc.EVEN)
+                assert int(host(ct)[0]) == t and np.array_equal(host(out), want), (n, off)
+                k = synth.uniform_u32(n, 4)
+                v = np.arange(n, dtype=np.uint32)
+                ko, vo = gc.split_radix(dev(k, off), dev(v, off), 0, 4)
+                wk, wv = orc.split_radix(k, v, 0, 4)
+                assert np.array_equal(host(ko), wk) and np.array_equal(host(vo), wv), (n, off)
+    finally:
+        gc.testing_force_fallback(False)

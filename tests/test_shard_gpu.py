@@ -6,9 +6,10 @@ concatenated result compared with the oracle on the whole array.
 On one GPU the exchange is the P pre-pass results written into the P slots of
 one device array; across GPUs it is the all-gather of partition_pass_tile_
 gb300.shard.gather_totals.  Shards start at arbitrary element offsets, so most
-of them are 4-byte but not 16-byte aligned and run the one-tile-per-CTA
-kernels, the others the persistent ones.  Bit-exact for integers, 1e-5
-relative (exact at a zero prefix) for float32 against the float64 oracle.
+of them are 4-byte but not 16-byte aligned and run the persistent kernels'
+shifted instantiations (staged from the 16-byte boundary below the shard),
+the others the aligned ones.  Bit-exact for integers, 1e-5 relative (exact at
+a zero prefix) for float32 against the float64 oracle.
 """
 
 import numpy as np

@@ -7,8 +7,9 @@ device.  This variant of select-if therefore keeps its scratch in a fixed
 array inside the library.  Its results must be the oracle's and those of
 gc_select_if, call after call: the shared array keeps the previous call's
 contents, and each call must clear what has to start at zero, on the
-persistent path (16-byte-aligned input, status words cleared in the kernel)
-and on the one-tile-per-CTA path (other inputs, cleared by a memset) alike.
+persistent path (status words cleared in the kernel) and on the
+one-tile-per-CTA path (taken when the device refuses a cooperative grid,
+forced here by a test hook; it clears the array with a memset) alike.
 This file sorts last so that a run stopping at the first failure has run
 every other test before it; it passes alone in a fresh process too.
 """
@@ -65,16 +66,21 @@ def _call(f, x_host, pred, offset):
 def test_noalloc_matches_oracle_and_select_if_on_consecutive_calls(orc):
     f = _entry()
     T = gc.tile_elements(gc.OP_SELECT_IF)
-    # Calls in a row with different sizes, dtypes, predicates and alignments:
-    # persistent, then one-tile-per-CTA (the array's memset path), then
-    # persistent again over the fallback's leftovers, and a smaller call
-    # whose stale status words lie beyond it.
-    cases = [("remove_zeros", 1_047_965, 0), ("u32_odd", 3 * T + 611, 1),
-             ("f32_nonzero", 100_003, 0), ("remove_zeros", 2 * T + 5, 1),
-             ("u32_odd", 5 * T, 0), ("f32_nonzero", 1_000, 1), ("remove_zeros", 1_047_965, 0)]
-    for kind, n, offset in cases:
+    # Calls in a row with different sizes, dtypes, predicates and pointer
+    # alignments: persistent, then one-tile-per-CTA (forced: the array's
+    # memset path), then persistent again over the fallback's leftovers, and
+    # smaller calls whose stale status words lie beyond them.
+    cases = [("remove_zeros", 1_047_965, 0, False), ("u32_odd", 3 * T + 611, 1, True),
+             ("f32_nonzero", 100_003, 0, False), ("remove_zeros", 2 * T + 5, 1, True),
+             ("u32_odd", 5 * T, 2, False), ("f32_nonzero", 1_000, 1, True),
+             ("remove_zeros", 1_047_965, 3, False)]
+    for kind, n, offset, fallback in cases:
         x, pred = _case(kind, n)
-        m, got, xd = _call(f, x, pred, offset)
+        gc.testing_force_fallback(fallback)
+        try:
+            m, got, xd = _call(f, x, pred, offset)
+        finally:
+            gc.testing_force_fallback(False)
         want = orc.select_if(x, pred)                        # the oracle
         assert m == want.shape[0], (kind, n, offset)
         assert np.array_equal(got[:m], want.view(np.uint32)), (kind, n, offset)
