@@ -18,14 +18,18 @@
 //   3. digit_scatter_kernel: every tile ranks its keys stably within the
 //      tile (warp by warp, 32 keys at a time: peers found by one ballot per
 //      digit bit, per-warp digit counters in shared memory), sorts them by
-//      digit in shared memory, and writes each digit's run to A[d * T + t]
-//      onwards, so consecutive threads store consecutive addresses.
+//      digit in shared memory as (key, payload) pairs, and writes each
+//      digit's run to A[d * T + t] onwards, so consecutive threads store
+//      consecutive addresses.  A full tile's keys and payloads are copied
+//      into shared memory by the TMA unit while the counters are cleared,
+//      so no payload load waits in the middle of the tile.
 //
 // Keys of int32 and float32 are sorted by the order-preserving key of
 // PredKeyBitClear, x ^ (signfill(x) & neg) ^ flip: its digits are computed
 // on the fly and the keys themselves move unchanged.
 #include "gc_device.cuh"
 #include "gc_internal.h"
+#include "gc_pipe.cuh"
 
 namespace {
 
@@ -34,19 +38,18 @@ using namespace gcd;
 constexpr int kDigitBits = 8;
 constexpr uint32_t kDigits = 1u << kDigitBits;
 constexpr int kDigitThreads = 256;  // one thread per digit in the per-digit steps
-constexpr int kDigitWarps = kDigitThreads / 32;
 constexpr int kDigitItems = 16;  // keys per thread
-constexpr uint32_t kSegment = 32u * kDigitItems;  // keys per warp, in order
 static_assert(kDigitThreads == int(kDigits), "one thread per digit");
 static_assert(gch::kDigitTile == kDigitThreads * kDigitItems, "tile size");
 
-// Digit of x at `shift` under the order-preserving key map.
+// Digit of x at `shift` (a multiple of 8) under the order-preserving key
+// map; the byte is taken with one permute.
 struct DigitOf {
     uint32_t neg, flip, shift;
     __device__ __forceinline__ uint32_t operator()(uint32_t x) const
     {
         const uint32_t key = x ^ ((uint32_t(int32_t(x) >> 31) & neg) ^ flip);
-        return (key >> shift) & (kDigits - 1u);
+        return __byte_perm(key, 0u, 0x4440u | (shift >> 3));
     }
 };
 
@@ -61,31 +64,31 @@ __device__ __forceinline__ uint32_t digit_peers(uint32_t d)
     for (int b = 0; b < BITS; ++b) {
         const uint32_t bit = (d >> b) & 1u;
         const uint32_t bal = __ballot_sync(kFullMask, bit != 0u);
-        m &= bal ^ (bit - 1u);  // bal where my bit is 1, ~bal where it is 0
+        m &= bal ^ (bit - 1u);
     }
     return m;
 }
 
 // Pass step 1: digit counts of tiles, written digit-major.  Each CTA counts
 // kCountTiles consecutive tiles, with the keys of all of them loaded before
-// the first is counted; shared-memory histograms are private to a warp and
-// a lane parity, so two lanes of one atomic instruction collide only when
-// they share both parity and digit.
+// the first is counted, by one shared-memory atomic per key.  The atomics'
+// rate sets the kernel's pace, so their bank conflicts are kept low (below).
 constexpr int kCountTiles = 2;
-constexpr int kCountHists = 2 * kDigitWarps;
 
 template <bool VEC>
 __global__ void __launch_bounds__(kDigitThreads)
 digit_count_kernel(const uint32_t *__restrict__ keys, uint32_t n, DigitOf dig,
                    uint32_t *__restrict__ counts, uint32_t tiles)
 {
-    __shared__ uint32_t s_hist[kCountTiles][kCountHists][kDigits];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int h = 2 * warp + (lane & 1);
+    // Eight sub-counts per digit, side by side, lane j counting into sub-count
+    // j & 7: the lanes of one atomic instruction meet in a bank only when they
+    // agree on j & 7 and on their digits' last two bits.
+    __shared__ __align__(16) uint32_t s_hist[kCountTiles][kDigits][8];
+    const int tid = threadIdx.x, lane = tid & 31;
 #pragma unroll
     for (int t = 0; t < kCountTiles; ++t)
 #pragma unroll
-        for (int w = 0; w < kCountHists; ++w) s_hist[t][w][tid] = 0u;
+        for (int j = 0; j < 8; ++j) (&s_hist[t][0][0])[j * kDigitThreads + tid] = 0u;
 
     constexpr int kVecs = kDigitItems / 4;  // 4-key vectors per thread per tile
     uint32_t x[kCountTiles][kVecs][4];
@@ -108,81 +111,115 @@ digit_count_kernel(const uint32_t *__restrict__ keys, uint32_t n, DigitOf dig,
             const uint32_t i = base + uint32_t(r) * (4u * kDigitThreads) + 4u * uint32_t(tid);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                if (full || i + q < n) atomicAdd(&s_hist[t][h][dig(x[t][r][q])], 1u);
+                if (full || i + q < n) atomicAdd(&s_hist[t][dig(x[t][r][q])][lane & 7], 1u);
         }
     }
     __syncthreads();
 #pragma unroll
     for (int t = 0; t < kCountTiles; ++t) {
         if (first + t < tiles) {
-            uint32_t c = 0u;
-#pragma unroll
-            for (int w = 0; w < kCountHists; ++w) c += s_hist[t][w][tid];
+            const uint4 a = *reinterpret_cast<const uint4 *>(&s_hist[t][tid][0]);
+            const uint4 b = *reinterpret_cast<const uint4 *>(&s_hist[t][tid][4]);
+            const uint32_t c = (a.x + a.y) + (a.z + a.w) + ((b.x + b.y) + (b.z + b.w));
             counts[size_t(tid) * tiles + first + t] = c;
         }
     }
 }
 
+// The scatter's CTA: kScatThreads threads, kScatItems keys each; warp w owns
+// keys [w * kScatSegment, (w + 1) * kScatSegment) of the tile, taken 32 at a
+// time in order (key j of the warp's step s is lane j).  Threads below
+// kDigits also do the per-digit steps.  256 threads x 16 keys at 4 CTAs per
+// SM (64 registers, about 50 KiB of shared memory each) beat 512 x 8 at 2
+// or 3 CTAs per SM.
+#ifndef GC_SCATTER_THREADS
+#define GC_SCATTER_THREADS 256
+#endif
+constexpr int kScatThreads = GC_SCATTER_THREADS;
+constexpr int kScatWarps = kScatThreads / 32;
+constexpr int kScatItems = int(gch::kDigitTile) / kScatThreads;
+constexpr uint32_t kScatSegment = 32u * kScatItems;
+static_assert(kScatThreads >= int(kDigits) && kScatItems % 4 == 0, "scatter shape");
+
+// Shared memory of the scatter (dynamic).  buf first receives the tile as
+// staged (payloads in buf[0, T) and keys in buf[T, 2T), T = kDigitTile; keys
+// only: buf[0, T)); once every thread holds its keys and payloads in
+// registers it receives the tile sorted by digit, as (key, payload) pairs
+// (keys only: keys).
+template <bool VALS>
 struct ScatterSmem {
-    uint32_t cnt[kDigitWarps][kDigits];  // per-warp running counts, then offsets
-    uint32_t start[kDigits];             // tile-local start of each digit's run
-    uint32_t glob[kDigits];              // global start of each digit's run
-    uint32_t warp_sum[kDigitWarps];
-    uint32_t keys[gch::kDigitTile];
+    // Per warp and digit: the digit's count so far.  Entry kDigits is the
+    // padding of the ragged tile.  After the scan: where the warp's first key
+    // of the digit goes in the sorted tile.
+    uint32_t cnt[kScatWarps][kDigits + 1];
+    uint32_t adj[kDigits];  // output index of sorted position 0 of each digit's run
+    uint32_t warp_sum[kDigits / 32];
+    uint64_t bar[2];        // TMA completion: keys, payloads
+    alignas(16) uint32_t buf[VALS ? 2 * gch::kDigitTile : gch::kDigitTile];
 };
 
-// Stable scatter of one tile by digit (FULL: all kDigitTile keys present).
-template <bool VALS, bool FULL>
+// Stable scatter of one tile by digit (FULL: all kDigitTile keys present;
+// TMA: a full tile's keys and payloads are being copied into buf).
+template <bool VALS, bool FULL, bool TMA>
 __device__ __forceinline__ void scatter_tile(const uint32_t *__restrict__ kin,
                                              const uint32_t *__restrict__ vin,
                                              uint32_t *__restrict__ kout, uint32_t *__restrict__ vout,
                                              uint32_t n, const DigitOf &dig, uint32_t tile,
-                                             uint32_t valid, uint8_t *ws, ScatterSmem &sm,
-                                             uint32_t *s_vals)
+                                             uint32_t valid, uint32_t glob, uint8_t *ws,
+                                             uint64_t timeout_ns, ScatterSmem<VALS> &sm)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t base = tile * gch::kDigitTile;
+    auto staged = [&](int s) -> uint32_t {
+        return uint32_t(warp) * kScatSegment + uint32_t(s) * 32u + uint32_t(lane);
+    };
 
-    // Warp w owns keys [w * kSegment, (w + 1) * kSegment) of the tile, taken
-    // 32 at a time in order: key j of the warp's step s is lane j.
-    uint32_t k[kDigitItems];
+    // Without the TMA copies the tile is staged into buf here with plain loads.
+    uint32_t *raw_k = sm.buf + (VALS ? gch::kDigitTile : 0u);
+    if (!TMA) {
 #pragma unroll
-    for (int s = 0; s < kDigitItems; ++s) {
-        const uint32_t li = uint32_t(warp) * kSegment + uint32_t(s) * 32u + uint32_t(lane);
-        k[s] = (FULL || li < valid) ? kin[base + li] : 0u;
+        for (int s = 0; s < kScatItems; ++s) {
+            const uint32_t li = staged(s);
+            raw_k[li] = (FULL || li < valid) ? kin[base + li] : 0u;
+            if (VALS) sm.buf[li] = (FULL || li < valid) ? vin[base + li] : 0u;
+        }
+        __syncwarp();  // each warp reads back only its own segment
+    } else {
+        mbar_wait(&sm.bar[0], 0u, ws, timeout_ns);
     }
     // Digits: packed four to a word in a full tile; whole words, with the
     // padding value kDigits past the end, in the ragged one.
-    uint32_t dg[FULL ? kDigitItems / 4 : kDigitItems];
+    uint32_t dg[FULL ? kScatItems / 4 : kScatItems];
 #pragma unroll
-    for (int s = 0; s < kDigitItems; ++s) {
+    for (int s = 0; s < kScatItems; ++s) {
+        const uint32_t li = staged(s);
+        const uint32_t d = dig(raw_k[li]);
         if (FULL) {
-            if ((s & 3) == 0) dg[s >> 2] = 0u;
-            dg[s >> 2] |= dig(k[s]) << (8 * (s & 3));
+            if ((s & 3) == 0) dg[s >> 2] = d;
+            else dg[s >> 2] |= d << (8 * (s & 3));
         } else {
-            const uint32_t li = uint32_t(warp) * kSegment + uint32_t(s) * 32u + uint32_t(lane);
-            dg[s] = li < valid ? dig(k[s]) : kDigits;
+            dg[s] = li < valid ? d : kDigits;
         }
     }
     auto digit = [&](int s) -> uint32_t {
-        return FULL ? (dg[s >> 2] >> (8 * (s & 3))) & (kDigits - 1u) : dg[s];
+        return FULL ? __byte_perm(dg[s >> 2], 0u, 0x4440u | uint32_t(s & 3)) : dg[s];
     };
-    __syncthreads();  // the counters are cleared
 
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    uint32_t *wcnt = sm.cnt[warp];
+    uint32_t rank2[kScatItems / 2];
     // Stable rank within the warp's segment: the peers of a key are the
     // lanes of its step with the same digit; the step's leader for each digit
     // (its lowest lane) adds the group to the warp's counter and keeps the old
-    // value for its peers.  Ranks (below kSegment) are kept two to a word.
-    const uint32_t lt_mask = (1u << lane) - 1u;
-    uint32_t rank2[kDigitItems / 2];
+    // value for its peers.  Ranks (below kScatSegment) are kept two to a word.
 #pragma unroll
-    for (int s = 0; s < kDigitItems; ++s) {
+    for (int s = 0; s < kScatItems; ++s) {
         const uint32_t ds = digit(s);
         const uint32_t peers = digit_peers<FULL ? kDigitBits : kDigitBits + 1>(ds);
         uint32_t before = 0u;
-        if ((peers & lt_mask) == 0u && (FULL || ds < kDigits)) {
-            before = sm.cnt[warp][ds];
-            sm.cnt[warp][ds] = before + uint32_t(__popc(peers));
+        if ((peers & lt_mask) == 0u) {
+            before = wcnt[ds];
+            wcnt[ds] = before + uint32_t(__popc(peers));
         }
         // The next step's leader for this digit may be another lane: order
         // this step's counter writes before its reads.
@@ -192,64 +229,77 @@ __device__ __forceinline__ void scatter_tile(const uint32_t *__restrict__ kin,
         else rank2[s >> 1] |= r << 16;
     }
     __syncthreads();
-    // The payloads are read only now, when the ranking no longer needs the
-    // registers; their latency overlaps the scans below.
-    uint32_t v[VALS ? kDigitItems : 1];
-    if (VALS) {
-#pragma unroll
-        for (int s = 0; s < kDigitItems; ++s) {
-            const uint32_t li = uint32_t(warp) * kSegment + uint32_t(s) * 32u + uint32_t(lane);
-            v[VALS ? s : 0] = (FULL || li < valid) ? vin[base + li] : 0u;
-        }
-    }
 
-    // Per digit (thread tid = digit): exclusive scan over the warps, then over
-    // the digits for the tile-local run starts.
-    uint32_t total = 0u;
+    // Per digit (threads below kDigits, thread = digit): exclusive scan over
+    // the warps, then over the digits for the tile-local run starts.
+    uint32_t total = 0u, incl = 0u;
+    if (tid < int(kDigits)) {
 #pragma unroll
-    for (int w = 0; w < kDigitWarps; ++w) {
-        const uint32_t c = sm.cnt[w][tid];
-        sm.cnt[w][tid] = total;
-        total += c;
-    }
-    uint32_t incl = total;
+        for (int w = 0; w < kScatWarps; ++w) {
+            const uint32_t c = sm.cnt[w][tid];
+            sm.cnt[w][tid] = total;
+            total += c;
+        }
+        incl = total;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(kFullMask, incl, o);
-        if (lane >= o) incl += y;
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFullMask, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) sm.warp_sum[warp] = incl;
     }
-    if (lane == 31) sm.warp_sum[warp] = incl;
+    // The keys and payloads, read back in the order of the ranks before the
+    // sorted tile overwrites them.
+    if (TMA && VALS) mbar_wait(&sm.bar[1], 0u, ws, timeout_ns);
+    uint32_t k[kScatItems], v[VALS ? kScatItems : 1];
+#pragma unroll
+    for (int s = 0; s < kScatItems; ++s) {
+        const uint32_t li = staged(s);
+        k[s] = raw_k[li];
+        if (VALS) v[VALS ? s : 0] = sm.buf[li];
+    }
     __syncthreads();
-    uint32_t wbase = 0u;
+    if (tid < int(kDigits)) {
+        uint32_t wbase = 0u;
 #pragma unroll
-    for (int w = 0; w < kDigitWarps; ++w) wbase += (w < warp) ? sm.warp_sum[w] : 0u;
-    sm.start[tid] = wbase + incl - total;
+        for (int w = 0; w < int(kDigits / 32); ++w) wbase += (w < warp) ? sm.warp_sum[w] : 0u;
+        const uint32_t start = wbase + incl - total;
+#pragma unroll
+        for (int w = 0; w < kScatWarps; ++w) sm.cnt[w][tid] += start;
+        sm.adj[tid] = glob - start;
+    }
     __syncthreads();
 
     // Tile-local sort by digit in shared memory.
 #pragma unroll
-    for (int s = 0; s < kDigitItems; ++s) {
+    for (int s = 0; s < kScatItems; ++s) {
         const uint32_t ds = digit(s);
         if (FULL || ds < kDigits) {
-            const uint32_t pos = sm.start[ds] + sm.cnt[warp][ds] + ((rank2[s >> 1] >> (16 * (s & 1))) & 0xffffu);
-            sm.keys[pos] = k[s];
-            if (VALS) s_vals[pos] = v[VALS ? s : 0];
+            const uint32_t pos = wcnt[ds] + ((rank2[s >> 1] >> (16 * (s & 1))) & 0xffffu);
+            if (VALS) reinterpret_cast<uint2 *>(sm.buf)[pos] = make_uint2(k[s], v[VALS ? s : 0]);
+            else sm.buf[pos] = k[s];
         }
     }
     __syncthreads();
 
     // Write out in sorted order: position i of the tile belongs to the run of
-    // its digit, which starts at start[digit] here and glob[digit] there.
+    // its digit, which starts at output index adj[digit] + (its start here).
 #pragma unroll
-    for (int s = 0; s < kDigitItems; ++s) {
-        const uint32_t i = uint32_t(s) * kDigitThreads + uint32_t(tid);
+    for (int s = 0; s < kScatItems; ++s) {
+        const uint32_t i = uint32_t(s) * kScatThreads + uint32_t(tid);
         if (FULL || i < valid) {
-            const uint32_t key = sm.keys[i];
-            const uint32_t dd = dig(key);
-            const uint32_t g = sm.glob[dd] + (i - sm.start[dd]);
+            uint32_t key, val = 0u;
+            if (VALS) {
+                const uint2 kv = reinterpret_cast<const uint2 *>(sm.buf)[i];
+                key = kv.x;
+                val = kv.y;
+            } else {
+                key = sm.buf[i];
+            }
+            const uint32_t g = sm.adj[dig(key)] + i;
             if (g < n) {
                 __stcs(kout + g, key);
-                if (VALS) __stcs(vout + g, s_vals[i]);
+                if (VALS) __stcs(vout + g, val);
             } else {
                 record_error(ws, kDeviceCheckCode, tile);  // a corrupted count table
             }
@@ -259,31 +309,62 @@ __device__ __forceinline__ void scatter_tile(const uint32_t *__restrict__ kin,
 
 // Pass step 3: stable scatter of one tile by digit.  offsets[d * T + t] is
 // where tile t's run of digit d starts in the output.
-// Resident CTAs per SM the scatter is compiled for (registers: 4 -> 64): the
-// kernel is latency-bound, and 4 CTAs per SM beat 2, 3 and 5.
 #ifndef GC_DIGIT_SCATTER_MIN_BLOCKS
 #define GC_DIGIT_SCATTER_MIN_BLOCKS 4
 #endif
 
-template <bool VALS>
-__global__ void __launch_bounds__(kDigitThreads, GC_DIGIT_SCATTER_MIN_BLOCKS)
+template <bool VALS, bool TMA>
+__global__ void __launch_bounds__(kScatThreads, GC_DIGIT_SCATTER_MIN_BLOCKS)
 digit_scatter_kernel(const uint32_t *__restrict__ kin, const uint32_t *__restrict__ vin,
                      uint32_t *__restrict__ kout, uint32_t *__restrict__ vout, uint32_t n,
                      DigitOf dig, const uint32_t *__restrict__ offsets, uint32_t tiles,
-                     uint8_t *ws)
+                     uint8_t *ws, uint64_t timeout_ns)
 {
-    __shared__ ScatterSmem sm;
-    __shared__ uint32_t s_vals[VALS ? gch::kDigitTile : 1];
+    extern __shared__ __align__(16) uint8_t scatter_smem[];
+    ScatterSmem<VALS> &sm = *reinterpret_cast<ScatterSmem<VALS> *>(scatter_smem);
     const int tid = threadIdx.x;
     const uint32_t tile = blockIdx.x;
     const uint32_t valid = min(gch::kDigitTile, n - tile * gch::kDigitTile);
-#pragma unroll
-    for (int w = 0; w < kDigitWarps; ++w) sm.cnt[w][tid] = 0u;
-    sm.glob[tid] = offsets[size_t(tid) * tiles + tile];
-    if (valid == gch::kDigitTile)
-        scatter_tile<VALS, true>(kin, vin, kout, vout, n, dig, tile, valid, ws, sm, s_vals);
+    const bool full = valid == gch::kDigitTile;
+    if (TMA && full && tid == 0) {
+        // Payloads into buf[0, T), keys into buf[T, 2T) (T = kDigitTile).
+        constexpr uint32_t kBytes = gch::kDigitTile * 4u;
+        const uint32_t base = tile * gch::kDigitTile;
+        mbar_init(&sm.bar[0], 1u);
+        if (VALS) mbar_init(&sm.bar[1], 1u);
+        fence_barrier_init();
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&sm.bar[0], kBytes);
+        bulk_load(sm.buf + (VALS ? gch::kDigitTile : 0u), kin + base, kBytes, &sm.bar[0]);
+        if (VALS) {
+            mbar_arrive_expect_tx(&sm.bar[1], kBytes);
+            bulk_load(sm.buf, vin + base, kBytes, &sm.bar[1]);
+        }
+    }
+    for (uint32_t i = uint32_t(tid); i < uint32_t(kScatWarps) * (kDigits + 1u); i += kScatThreads)
+        (&sm.cnt[0][0])[i] = 0u;
+    const uint32_t glob = tid < int(kDigits) ? offsets[size_t(tid) * tiles + tile] : 0u;
+    __syncthreads();  // counters cleared, barriers initialised
+    if (!full)
+        scatter_tile<VALS, false, false>(kin, vin, kout, vout, n, dig, tile, valid, glob, ws, timeout_ns, sm);
+    else if (TMA)
+        scatter_tile<VALS, true, true>(kin, vin, kout, vout, n, dig, tile, valid, glob, ws, timeout_ns, sm);
     else
-        scatter_tile<VALS, false>(kin, vin, kout, vout, n, dig, tile, valid, ws, sm, s_vals);
+        scatter_tile<VALS, true, false>(kin, vin, kout, vout, n, dig, tile, valid, glob, ws, timeout_ns, sm);
+}
+
+template <bool VALS, bool TMA>
+cudaError_t launch_scatter(const uint32_t *kin, const uint32_t *vin, uint32_t *kout, uint32_t *vout,
+                           uint32_t n, const DigitOf &dig, const uint32_t *table, uint32_t tiles,
+                           uint8_t *ws, cudaStream_t s, const gch::LaunchOpts &o)
+{
+    constexpr size_t kSmem = sizeof(ScatterSmem<VALS>);
+    auto kern = digit_scatter_kernel<VALS, TMA>;
+    // Sets the kernel's shared-memory limit, once per device.
+    if (gch::persistent_grid(reinterpret_cast<const void *>(kern), kScatThreads, kSmem, tiles) <= 0)
+        return cudaErrorInvalidConfiguration;
+    kern<<<tiles, kScatThreads, kSmem, s>>>(kin, vin, kout, vout, n, dig, table, tiles, ws, o.timeout_ns);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -321,12 +402,15 @@ cudaError_t launch_radix_sort_digits(const uint32_t *keys_in, const uint32_t *va
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         e = launch_scan(table, table, scan_total, tiles * kDigits, GC_U32, ws, s, o, false);
         if (e != cudaSuccess) return e;
+        // Full tiles are staged by TMA when the sources are 16-byte aligned.
+        const bool tma = aligned16(src_k) && (!vals || aligned16(src_v));
         if (vals)
-            digit_scatter_kernel<true><<<tiles, kDigitThreads, 0, s>>>(src_k, src_v, dst_k, dst_v, n,
-                                                                       dig, table, tiles, ws);
+            e = tma ? launch_scatter<true, true>(src_k, src_v, dst_k, dst_v, n, dig, table, tiles, ws, s, o)
+                    : launch_scatter<true, false>(src_k, src_v, dst_k, dst_v, n, dig, table, tiles, ws, s, o);
         else
-            digit_scatter_kernel<false><<<tiles, kDigitThreads, 0, s>>>(src_k, nullptr, dst_k, nullptr,
-                                                                        n, dig, table, tiles, ws);
+            e = tma ? launch_scatter<false, true>(src_k, nullptr, dst_k, nullptr, n, dig, table, tiles, ws, s, o)
+                    : launch_scatter<false, false>(src_k, nullptr, dst_k, nullptr, n, dig, table, tiles, ws, s, o);
+        if (e != cudaSuccess) return e;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         src_k = dst_k;
         src_v = dst_v;
