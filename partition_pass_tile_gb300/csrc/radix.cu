@@ -26,7 +26,8 @@
 //
 // Keys of int32 and float32 are sorted by the order-preserving key of
 // PredKeyBitClear, x ^ (signfill(x) & neg) ^ flip: its digits are computed
-// on the fly and the keys themselves move unchanged.
+// on the fly, by code specialised to the dtype's map, and the keys
+// themselves move unchanged.
 #include "gc_device.cuh"
 #include "gc_internal.h"
 #include "gc_pipe.cuh"
@@ -42,14 +43,21 @@ constexpr int kDigitItems = 16;  // keys per thread
 static_assert(kDigitThreads == int(kDigits), "one thread per digit");
 static_assert(gch::kDigitTile == kDigitThreads * kDigitItems, "tile size");
 
-// Digit of x at `shift` (a multiple of 8) under the order-preserving key
-// map; the byte is taken with one permute.
+// Digit of x under the order-preserving key map of its dtype: one of the
+// key's bytes, taken with one permute (sel = 0x4440 | byte index).  uint32
+// keys are their own key; int32 keys flip the sign bit; float32 keys flip
+// every bit of a negative value and the sign bit of any other.
+enum class KeyKind { U32, I32, F32 };
+
+template <KeyKind K>
 struct DigitOf {
-    uint32_t neg, flip, shift;
+    uint32_t sel;
     __device__ __forceinline__ uint32_t operator()(uint32_t x) const
     {
-        const uint32_t key = x ^ ((uint32_t(int32_t(x) >> 31) & neg) ^ flip);
-        return __byte_perm(key, 0u, 0x4440u | (shift >> 3));
+        uint32_t key = x;
+        if constexpr (K == KeyKind::I32) key = x ^ 0x80000000u;
+        if constexpr (K == KeyKind::F32) key = x ^ (uint32_t(int32_t(x) >> 31) | 0x80000000u);
+        return __byte_perm(key, 0u, sel);
     }
 };
 
@@ -73,11 +81,11 @@ __device__ __forceinline__ uint32_t digit_peers(uint32_t d)
 // kCountTiles consecutive tiles, with the keys of all of them loaded before
 // the first is counted, by one shared-memory atomic per key.  The atomics'
 // rate sets the kernel's pace, so their bank conflicts are kept low (below).
-constexpr int kCountTiles = 2;
+constexpr int kCountTiles = 2;  // 2 beat 1 and 4
 
-template <bool VEC>
+template <class Dig, bool VEC>
 __global__ void __launch_bounds__(kDigitThreads)
-digit_count_kernel(const uint32_t *__restrict__ keys, uint32_t n, DigitOf dig,
+digit_count_kernel(const uint32_t *__restrict__ keys, uint32_t n, Dig dig,
                    uint32_t *__restrict__ counts, uint32_t tiles)
 {
     // Eight sub-counts per digit, side by side, lane j counting into sub-count
@@ -160,11 +168,11 @@ struct ScatterSmem {
 
 // Stable scatter of one tile by digit (FULL: all kDigitTile keys present;
 // TMA: a full tile's keys and payloads are being copied into buf).
-template <bool VALS, bool FULL, bool TMA>
+template <bool VALS, bool FULL, bool TMA, class Dig>
 __device__ __forceinline__ void scatter_tile(const uint32_t *__restrict__ kin,
                                              const uint32_t *__restrict__ vin,
                                              uint32_t *__restrict__ kout, uint32_t *__restrict__ vout,
-                                             uint32_t n, const DigitOf &dig, uint32_t tile,
+                                             uint32_t n, const Dig &dig, uint32_t tile,
                                              uint32_t valid, uint32_t glob, uint8_t *ws,
                                              uint64_t timeout_ns, ScatterSmem<VALS> &sm)
 {
@@ -313,11 +321,11 @@ __device__ __forceinline__ void scatter_tile(const uint32_t *__restrict__ kin,
 #define GC_DIGIT_SCATTER_MIN_BLOCKS 4
 #endif
 
-template <bool VALS, bool TMA>
+template <class Dig, bool VALS, bool TMA>
 __global__ void __launch_bounds__(kScatThreads, GC_DIGIT_SCATTER_MIN_BLOCKS)
 digit_scatter_kernel(const uint32_t *__restrict__ kin, const uint32_t *__restrict__ vin,
                      uint32_t *__restrict__ kout, uint32_t *__restrict__ vout, uint32_t n,
-                     DigitOf dig, const uint32_t *__restrict__ offsets, uint32_t tiles,
+                     Dig dig, const uint32_t *__restrict__ offsets, uint32_t tiles,
                      uint8_t *ws, uint64_t timeout_ns)
 {
     extern __shared__ __align__(16) uint8_t scatter_smem[];
@@ -353,13 +361,13 @@ digit_scatter_kernel(const uint32_t *__restrict__ kin, const uint32_t *__restric
         scatter_tile<VALS, true, false>(kin, vin, kout, vout, n, dig, tile, valid, glob, ws, timeout_ns, sm);
 }
 
-template <bool VALS, bool TMA>
+template <class Dig, bool VALS, bool TMA>
 cudaError_t launch_scatter(const uint32_t *kin, const uint32_t *vin, uint32_t *kout, uint32_t *vout,
-                           uint32_t n, const DigitOf &dig, const uint32_t *table, uint32_t tiles,
+                           uint32_t n, const Dig &dig, const uint32_t *table, uint32_t tiles,
                            uint8_t *ws, cudaStream_t s, const gch::LaunchOpts &o)
 {
     constexpr size_t kSmem = sizeof(ScatterSmem<VALS>);
-    auto kern = digit_scatter_kernel<VALS, TMA>;
+    auto kern = digit_scatter_kernel<Dig, VALS, TMA>;
     // Sets the kernel's shared-memory limit, once per device.
     if (gch::persistent_grid(reinterpret_cast<const void *>(kern), kScatThreads, kSmem, tiles) <= 0)
         return cudaErrorInvalidConfiguration;
@@ -367,21 +375,20 @@ cudaError_t launch_scatter(const uint32_t *kin, const uint32_t *vin, uint32_t *k
     return cudaGetLastError();
 }
 
-}  // namespace
-
-namespace gch {
-
-cudaError_t launch_radix_sort_digits(const uint32_t *keys_in, const uint32_t *vals_in,
-                                     uint32_t *keys_out, uint32_t *vals_out, uint32_t n,
-                                     uint32_t key_neg, uint32_t key_flip, uint8_t *ws,
-                                     cudaStream_t s, const LaunchOpts &o)
+// The four passes of one sort, keys mapped to their order-preserving keys
+// by Dig.
+template <KeyKind K>
+cudaError_t sort_digits(const uint32_t *keys_in, const uint32_t *vals_in, uint32_t *keys_out,
+                        uint32_t *vals_out, uint32_t n, uint8_t *ws, cudaStream_t s,
+                        const gch::LaunchOpts &o)
 {
+    using Dig = DigitOf<K>;
     const bool vals = vals_in != nullptr;
-    const uint32_t tiles = uint32_t(ceil_div(n, kDigitTile));
-    uint32_t *tmp_k = reinterpret_cast<uint32_t *>(ws + radix_temp_offset(n));
-    uint32_t *tmp_v = reinterpret_cast<uint32_t *>(ws + radix_temp_offset(n) + radix_temp_stride(n));
-    uint32_t *table = reinterpret_cast<uint32_t *>(ws + digit_table_offset(n));
-    uint32_t *scan_total = reinterpret_cast<uint32_t *>(ws + kHdrDigitScanTotal);
+    const uint32_t tiles = uint32_t(gch::ceil_div(n, gch::kDigitTile));
+    uint32_t *tmp_k = reinterpret_cast<uint32_t *>(ws + gch::radix_temp_offset(n));
+    uint32_t *tmp_v = reinterpret_cast<uint32_t *>(ws + gch::radix_temp_offset(n) + gch::radix_temp_stride(n));
+    uint32_t *table = reinterpret_cast<uint32_t *>(ws + gch::digit_table_offset(n));
+    uint32_t *scan_total = reinterpret_cast<uint32_t *>(ws + gch::kHdrDigitScanTotal);
     constexpr int kPasses = 32 / kDigitBits;
     static_assert(kPasses % 2 == 0, "an even pass count ends in the output buffers");
 
@@ -393,29 +400,47 @@ cudaError_t launch_radix_sort_digits(const uint32_t *keys_in, const uint32_t *va
         // (also when the input is the output).
         uint32_t *dst_k = (p % 2 == 0) ? tmp_k : keys_out;
         uint32_t *dst_v = vals ? ((p % 2 == 0) ? tmp_v : vals_out) : nullptr;
-        const DigitOf dig{key_neg, key_flip, uint32_t(p * kDigitBits)};
-        const uint32_t count_grid = uint32_t(ceil_div(tiles, kCountTiles));
-        if (aligned16(src_k))
-            digit_count_kernel<true><<<count_grid, kDigitThreads, 0, s>>>(src_k, n, dig, table, tiles);
+        const Dig dig{0x4440u | uint32_t(p)};  // byte p of the key
+        const uint32_t count_grid = uint32_t(gch::ceil_div(tiles, kCountTiles));
+        if (gch::aligned16(src_k))
+            digit_count_kernel<Dig, true><<<count_grid, kDigitThreads, 0, s>>>(src_k, n, dig, table, tiles);
         else
-            digit_count_kernel<false><<<count_grid, kDigitThreads, 0, s>>>(src_k, n, dig, table, tiles);
+            digit_count_kernel<Dig, false><<<count_grid, kDigitThreads, 0, s>>>(src_k, n, dig, table, tiles);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        e = launch_scan(table, table, scan_total, tiles * kDigits, GC_U32, ws, s, o, false);
+        e = gch::launch_scan(table, table, scan_total, tiles * kDigits, GC_U32, ws, s, o, false);
         if (e != cudaSuccess) return e;
         // Full tiles are staged by TMA when the sources are 16-byte aligned.
-        const bool tma = aligned16(src_k) && (!vals || aligned16(src_v));
+        const bool tma = gch::aligned16(src_k) && (!vals || gch::aligned16(src_v));
         if (vals)
-            e = tma ? launch_scatter<true, true>(src_k, src_v, dst_k, dst_v, n, dig, table, tiles, ws, s, o)
-                    : launch_scatter<true, false>(src_k, src_v, dst_k, dst_v, n, dig, table, tiles, ws, s, o);
+            e = tma ? launch_scatter<Dig, true, true>(src_k, src_v, dst_k, dst_v, n, dig, table, tiles, ws, s, o)
+                    : launch_scatter<Dig, true, false>(src_k, src_v, dst_k, dst_v, n, dig, table, tiles, ws, s, o);
         else
-            e = tma ? launch_scatter<false, true>(src_k, nullptr, dst_k, nullptr, n, dig, table, tiles, ws, s, o)
-                    : launch_scatter<false, false>(src_k, nullptr, dst_k, nullptr, n, dig, table, tiles, ws, s, o);
+            e = tma ? launch_scatter<Dig, false, true>(src_k, nullptr, dst_k, nullptr, n, dig, table, tiles, ws, s, o)
+                    : launch_scatter<Dig, false, false>(src_k, nullptr, dst_k, nullptr, n, dig, table, tiles, ws, s, o);
         if (e != cudaSuccess) return e;
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
         src_k = dst_k;
         src_v = dst_v;
     }
     return cudaSuccess;
+}
+
+}  // namespace
+
+namespace gch {
+
+cudaError_t launch_radix_sort_digits(const uint32_t *keys_in, const uint32_t *vals_in,
+                                     uint32_t *keys_out, uint32_t *vals_out, uint32_t n,
+                                     uint32_t key_neg, uint32_t key_flip, uint8_t *ws,
+                                     cudaStream_t s, const LaunchOpts &o)
+{
+    // The three order-preserving key maps x ^ (signfill(x) & neg) ^ flip.
+    if (key_neg == 0u && key_flip == 0u)
+        return sort_digits<KeyKind::U32>(keys_in, vals_in, keys_out, vals_out, n, ws, s, o);
+    if (key_neg == 0u && key_flip == 0x80000000u)
+        return sort_digits<KeyKind::I32>(keys_in, vals_in, keys_out, vals_out, n, ws, s, o);
+    if (key_neg == 0x7FFFFFFFu && key_flip == 0x80000000u)
+        return sort_digits<KeyKind::F32>(keys_in, vals_in, keys_out, vals_out, n, ws, s, o);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace gch
