@@ -491,32 +491,45 @@ def run_gc(args):
     del out_s
 
     # End to end: every step copies its inputs in from pinned host memory and
-    # every output (and the counts) back, through the C ABI.  Three streams:
-    # host-to-device copies, the kernels, device-to-host copies, ordered by
-    # events.  Device inputs are double-buffered by step parity, so the copies
-    # of step k + 1 run while step k computes; each op has its own device
-    # output, copied back while the next op runs.
+    # its results back, through the C ABI.  Three streams: host-to-device
+    # copies, the kernels, device-to-host copies, ordered by events.  Device
+    # inputs are double-buffered by step parity, so the copies of step k + 1
+    # run while step k computes.  An op with a fixed-size result (the scans,
+    # the partition, the sort's keys and payloads) is copied back whole as
+    # soon as it is done.  A select's result is its first `count` elements:
+    # the host reads step k's counts (copied to pinned memory on the kernel
+    # stream) while step k + 1 is already queued, then copies back exactly
+    # those elements; select outputs are double-buffered by step parity so
+    # step k + 1 does not overwrite them first.  (Double-buffering every
+    # output as well measured slower: 55.1 against 52.4 ms per step, the
+    # copies in both directions then overlapping the kernels more and each
+    # running slower.)
     pinned = {k: torch.from_numpy(v.view(np.int32) if v.dtype == np.uint32 else v).pin_memory()
               for k, v in h.items()}
     d_in = [d, {k: torch.empty_like(v) for k, v in d.items()}]
-    outs = {name: torch.empty(n, dtype=torch.int32, device=dev) for name in OPS}
+    SELECTS = ("select_p01", "select_p50", "select_p99", "atomic_tile_p50")
+    COUNT_SLOT = {"select_p01": 2, "select_p50": 3, "select_p99": 4, "atomic_tile_p50": 7}
+    outs = [{name: torch.empty(n, dtype=torch.int32, device=dev) for name in OPS}, {}]
+    outs[1] = {name: (torch.empty(n, dtype=torch.int32, device=dev) if name in SELECTS else outs[0][name])
+               for name in OPS}
     out_vals = torch.empty(n, dtype=torch.int32, device=dev)
     host_outs = {name: torch.empty(n, dtype=torch.int32).pin_memory() for name in OPS}
     host_vals = torch.empty(n, dtype=torch.int32).pin_memory()
-    host_counts = torch.empty(8, dtype=torch.int32).pin_memory()
+    host_counts = [torch.empty(8, dtype=torch.int32).pin_memory() for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
-    d2h = sum(4 * n for _ in OPS) + 4 * n + host_counts.numel() * 4
     s_h2d = torch.cuda.Stream(device=dev)
     s_d2h = torch.cuda.Stream(device=dev)
+    s_sel = torch.cuda.Stream(device=dev)  # survivors: not queued behind the next step's copies
     inputs_of = {"scan_i32": ["x"], "scan_f32": ["f"], "select_p01": ["s01"],
                  "select_p50": ["s50"], "select_p99": ["s99"], "partition": ["x"],
                  "radix32": ["x", "payload"], "atomic_tile_p50": ["s50"]}
     set_free = [None, None]  # event: the compute stream is done with an input set
-    out_free = {name: None for name in OPS}  # event: an op's output has been copied back
+    out_free = [{name: None for name in OPS}, {name: None for name in OPS}]  # copied back
+    pending = []             # (parity, counts-copied event) of steps whose selects await copy-back
+    d2h_total = [0]
 
-    def e2e_ops(dd):
+    def e2e_ops(dd, o, ov):
         xk = dd["x"].view(torch.uint32)
-        o = outs
         return {
             "scan_i32": lambda: gc.exclusive_scan(dd["x"], out=o["scan_i32"], total=counts[0:1].view(torch.int32), ws=ws, stream=stream),
             "scan_f32": lambda: gc.exclusive_scan(dd["f"], out=o["scan_f32"].view(torch.float32), total=counts[1:2].view(torch.float32), ws=ws, stream=stream),
@@ -525,9 +538,23 @@ def run_gc(args):
             "select_p99": lambda: gc.select_if(dd["s99"], "nonzero", out=o["select_p99"], count=counts[4:5], ws=ws, stream=stream),
             "partition": lambda: gc.partition(dd["x"], "even", out=o["partition"], count_true=counts[5:6], ws=ws, stream=stream),
             "radix32": lambda: gc.split_radix(xk, dd["payload"], 0, 32, keys_out=o["radix32"].view(torch.uint32),
-                                              vals_out=out_vals.view(torch.uint32), ws=ws, stream=stream),
+                                              vals_out=ov.view(torch.uint32), ws=ws, stream=stream),
             "atomic_tile_p50": lambda: gc.select_if_atomic(dd["s50"], "nonzero", out=o["atomic_tile_p50"], count=counts[7:8], ws=ws, stream=stream, per_tile=True),
         }
+
+    def copy_back_selects(par, ready):
+        """Step with parity `par` finished: copy back each select's survivors."""
+        ready.synchronize()
+        c = host_counts[par].numpy().view(np.uint32)
+        s_sel.wait_event(ready)
+        for name in SELECTS:
+            m = int(c[COUNT_SLOT[name]])
+            with torch.cuda.stream(s_sel):
+                host_outs[name][:m].copy_(outs[par][name][:m], non_blocking=True)
+            d2h_total[0] += 4 * m
+            freed = torch.cuda.Event()
+            freed.record(s_sel)
+            out_free[par][name] = freed
 
     def e2e_step(k):
         par = k % 2
@@ -542,49 +569,73 @@ def run_gc(args):
             ev = torch.cuda.Event()
             ev.record(s_h2d)
             arrived[key] = ev
-        calls = e2e_ops(dd)
+        calls = e2e_ops(dd, outs[par], out_vals)
         for name in OPS:
             for key in inputs_of[name]:
                 stream.wait_event(arrived[key])
-            if out_free[name] is not None:
-                stream.wait_event(out_free[name])
+            if out_free[par][name] is not None:
+                stream.wait_event(out_free[par][name])
             calls[name]()
+            if name in SELECTS:
+                continue
             done = torch.cuda.Event()
             done.record(stream)
             s_d2h.wait_event(done)
             with torch.cuda.stream(s_d2h):
-                host_outs[name].copy_(outs[name], non_blocking=True)
+                host_outs[name].copy_(outs[par][name], non_blocking=True)
+                d2h_total[0] += 4 * n
                 if name == "radix32":
                     host_vals.copy_(out_vals, non_blocking=True)
+                    d2h_total[0] += 4 * n
             freed = torch.cuda.Event()
             freed.record(s_d2h)
-            out_free[name] = freed
+            for q in (0, 1):
+                out_free[q][name] = freed  # one buffer serves both parities
         consumed = torch.cuda.Event()
         consumed.record(stream)
         set_free[par] = consumed
-        s_d2h.wait_event(consumed)
-        with torch.cuda.stream(s_d2h):
-            host_counts.copy_(counts.view(torch.int32), non_blocking=True)
+        with torch.cuda.stream(stream):
+            host_counts[par].copy_(counts.view(torch.int32), non_blocking=True)
+        d2h_total[0] += 4 * host_counts[par].numel()
+        ready = torch.cuda.Event()
+        ready.record(stream)
+        pending.append((par, ready))
+        if len(pending) > 1:  # the previous step's selects, while this step is queued
+            copy_back_selects(*pending.pop(0))
+
+    def drain():
+        while pending:
+            copy_back_selects(*pending.pop(0))
 
     e2e_step(0)
     e2e_step(1)
+    drain()
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
+    d2h_total[0] = 0
     e0.record(s_h2d)
     stream.wait_event(e0)
     s_d2h.wait_event(e0)
+    s_sel.wait_event(e0)
     for k in range(args.steps):
         e2e_step(k)
+    drain()
+    sel_done = torch.cuda.Event()
+    sel_done.record(s_sel)
+    s_d2h.wait_event(sel_done)
     e1.record(s_d2h)  # the last copy back depends on every copy in and every kernel
     torch.cuda.synchronize(dev)
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
-    # the copied-back counts are the true ones (the step really ran)
-    hc = host_counts.numpy().view(np.uint32)
+    d2h = d2h_total[0] / args.steps
+    # the copied-back counts and survivors are the true ones (the step really ran)
+    hc = host_counts[(args.steps - 1) % 2].numpy().view(np.uint32)
     assert int(hc[3]) == kept["select_p50"] and int(hc[7]) == kept["atomic_tile_p50"]
+    m01 = int(hc[2])
+    assert np.array_equal(host_outs["select_p01"][:m01].numpy(), h["s01"][h["s01"] != 0].view(np.int32))
 
     peak, peak_kind = read_peaks()
     elems_step = len(OPS) * n
@@ -646,8 +697,9 @@ def run_gc(args):
                 "unit": "Gelem/s", "ms_per_step": round(e2e_ms, 3),
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "path": "pinned host inputs -> H2D (own stream, inputs double-buffered by step) -> "
-                        "gc_* through the C ABI -> D2H of every output and the counts (own "
-                        "stream), every step"},
+                        "gc_* through the C ABI -> D2H (own stream) of every result: the scans, the "
+                        "partition, the sort's keys and payloads whole, each select's count survivors "
+                        "(counts read one step late), every step"},
         "gpu_launches": sum(LAUNCHES_PER_OP.values()) * args.steps,
     }
     if rank == 0:
