@@ -500,19 +500,20 @@ def run_gc(args):
     # the host reads step k's counts (copied to pinned memory on the kernel
     # stream) while step k + 1 is already queued, then copies back exactly
     # those elements; select outputs are double-buffered by step parity so
-    # step k + 1 does not overwrite them first.  (Double-buffering every
-    # output as well measured slower: 55.1 against 52.4 ms per step, the
-    # copies in both directions then overlapping the kernels more and each
-    # running slower.)
+    # step k + 1 does not overwrite them first.  The sort's outputs are
+    # double-buffered too: otherwise each step's 22 ms sort would wait for the
+    # previous step's 2 GB of keys and payloads to be copied back, and the
+    # step would become that chain.
     pinned = {k: torch.from_numpy(v.view(np.int32) if v.dtype == np.uint32 else v).pin_memory()
               for k, v in h.items()}
     d_in = [d, {k: torch.empty_like(v) for k, v in d.items()}]
     SELECTS = ("select_p01", "select_p50", "select_p99", "atomic_tile_p50")
     COUNT_SLOT = {"select_p01": 2, "select_p50": 3, "select_p99": 4, "atomic_tile_p50": 7}
+    DOUBLE = SELECTS + ("radix32",)
     outs = [{name: torch.empty(n, dtype=torch.int32, device=dev) for name in OPS}, {}]
-    outs[1] = {name: (torch.empty(n, dtype=torch.int32, device=dev) if name in SELECTS else outs[0][name])
+    outs[1] = {name: (torch.empty(n, dtype=torch.int32, device=dev) if name in DOUBLE else outs[0][name])
                for name in OPS}
-    out_vals = torch.empty(n, dtype=torch.int32, device=dev)
+    out_vals = [torch.empty(n, dtype=torch.int32, device=dev) for _ in range(2)]
     host_outs = {name: torch.empty(n, dtype=torch.int32).pin_memory() for name in OPS}
     host_vals = torch.empty(n, dtype=torch.int32).pin_memory()
     host_counts = [torch.empty(8, dtype=torch.int32).pin_memory() for _ in range(2)]
@@ -569,7 +570,7 @@ def run_gc(args):
             ev = torch.cuda.Event()
             ev.record(s_h2d)
             arrived[key] = ev
-        calls = e2e_ops(dd, outs[par], out_vals)
+        calls = e2e_ops(dd, outs[par], out_vals[par])
         for name in OPS:
             for key in inputs_of[name]:
                 stream.wait_event(arrived[key])
@@ -585,12 +586,12 @@ def run_gc(args):
                 host_outs[name].copy_(outs[par][name], non_blocking=True)
                 d2h_total[0] += 4 * n
                 if name == "radix32":
-                    host_vals.copy_(out_vals, non_blocking=True)
+                    host_vals.copy_(out_vals[par], non_blocking=True)
                     d2h_total[0] += 4 * n
             freed = torch.cuda.Event()
             freed.record(s_d2h)
-            for q in (0, 1):
-                out_free[q][name] = freed  # one buffer serves both parities
+            for q in ((par,) if name in DOUBLE else (0, 1)):
+                out_free[q][name] = freed  # one buffer serves both parities unless doubled
         consumed = torch.cuda.Event()
         consumed.record(stream)
         set_free[par] = consumed
