@@ -138,7 +138,7 @@ digit_count_kernel(const uint32_t *__restrict__ keys, uint32_t n, Dig dig,
 // keys [w * kScatSegment, (w + 1) * kScatSegment) of the tile, taken 32 at a
 // time in order (key j of the warp's step s is lane j).  Threads below
 // kDigits also do the per-digit steps.  256 threads x 16 keys at 4 CTAs per
-// SM (64 registers, about 50 KiB of shared memory each) beat 512 x 8 at 2
+// SM (64 registers, 42 KiB of shared memory each) beat 512 x 8 at 2
 // or 3 CTAs per SM.
 #ifndef GC_SCATTER_THREADS
 #define GC_SCATTER_THREADS 256
