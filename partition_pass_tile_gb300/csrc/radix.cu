@@ -278,10 +278,13 @@ __device__ __forceinline__ void scatter_tile(const uint32_t *__restrict__ kin,
     }
     __syncthreads();
 
-    // Tile-local sort by digit in shared memory.
+    // Tile-local sort by digit in shared memory.  With payloads each key's
+    // digit is computed again here, so the packed digits die after the
+    // ranking and the payloads fit in registers without spills (5.49 -> 5.34
+    // ms per float32 sort with payloads at 2^28); keys alone keep them.
 #pragma unroll
     for (int s = 0; s < kScatItems; ++s) {
-        const uint32_t ds = digit(s);
+        const uint32_t ds = VALS ? (FULL || staged(s) < valid ? dig(k[s]) : kDigits) : digit(s);
         if (FULL || ds < kDigits) {
             const uint32_t pos = wcnt[ds] + ((rank2[s >> 1] >> (16 * (s & 1))) & 0xffffu);
             if (VALS) reinterpret_cast<uint2 *>(sm.buf)[pos] = make_uint2(k[s], v[VALS ? s : 0]);
